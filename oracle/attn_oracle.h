@@ -1,0 +1,64 @@
+/*
+ * attn_oracle.h -- plain, slow, fp64 CPU oracle for scaled dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path may link, load or call
+ * this library; only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do. It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (the plain definition, per batch b, head h and query row i):
+ *   Eq. (1)  Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V
+ *     -- "Attention Is All You Need" (rockcohen.cc), section 5.1 "scaled
+ *        dot-product attention"; vlmlib.cn paper summary, "scaled dot-product
+ *        attention"; attention-paper-guide, section 03.2.
+ *   Illegal connections get -inf at the softmax INPUT, so their weight is an
+ *   exact 0 -- rockcohen.cc sections 5.3 and 6.3.
+ *   Causal (decoder self-attention): key j is illegal for query i when j > i.
+ *   Key padding (encoder, cross-attention): key j is illegal when j >= key_lens[b]
+ *   (right padding; the reading of the csdn blog's padding mask, see DESIGN).
+ *
+ * Conventions chosen where the pages are silent:
+ *   - a row with no legal key returns o = 0 and lse = -inf;
+ *   - lse_i = ln sum_{j legal} exp(scale * q_i . k_j)  (natural log);
+ *   - scale is used exactly as given (callers pass 1/sqrt(d_k)).
+ *
+ * Layouts: Q [B,H,n_q,d_k], K [B,H,n_k,d_k], V [B,H,n_k,d_v], O [B,H,n_q,d_v],
+ * all contiguous row-major, the per-head layout of the csdn blog's split_heads.
+ */
+#ifndef ATTN_ORACLE_H
+#define ATTN_ORACLE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element type of the Q/K/V input arrays */
+enum { ORACLE_F64 = 0, ORACLE_F32 = 1, ORACLE_BF16 = 2 /* raw bf16 bit patterns, uint16 */ };
+/* mask bits */
+enum { ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_KEY_PADDING = 2 };
+
+/* Full output. out: B*H*n_q*d_v doubles; lse: B*H*n_q doubles or NULL.
+ * key_lens: B ints, required iff mask bit 2 is set. n_threads <= 0 means 1.
+ * Returns 0, or -1 on an invalid argument. */
+int oracle_attn(const void* q, const void* k, const void* v, int dtype,
+                int B, int H, int n_q, int n_k, int d_k, int d_v, double scale,
+                int mask_mode, const int* key_lens,
+                double* out, double* lse, int n_threads);
+
+/* A subset of query rows. row_ids[r] = (b*H + h)*n_q + i. out_rows: n_rows*d_v,
+ * lse_rows: n_rows (or NULL). Same semantics as oracle_attn for those rows. */
+int oracle_attn_rows(const void* q, const void* k, const void* v, int dtype,
+                     int B, int H, int n_q, int n_k, int d_k, int d_v, double scale,
+                     int mask_mode, const int* key_lens,
+                     long long n_rows, const long long* row_ids,
+                     double* out_rows, double* lse_rows, int n_threads);
+
+/* The softmax weight matrix A = softmax(scale * Q K^T + mask): B*H*n_q*n_k doubles.
+ * Illegal entries are exactly 0.0; a row with no legal key is all zeros. */
+int oracle_attn_weights(const void* q, const void* k, int dtype,
+                        int B, int H, int n_q, int n_k, int d_k, double scale,
+                        int mask_mode, const int* key_lens, double* weights);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,278 @@
+"""Pins that tie the fp64 oracle to something other than itself.
+
+Each pin takes an ``oracle.Oracle`` and raises ``AssertionError`` when the oracle
+disagrees with what the pages or the mathematics fix: values the pages print for
+their worked examples (``tests/golden``), closed forms, invariants, special cases
+that reduce to a library routine, and brute force on tiny inputs. The pins are
+chosen so that a plausible slip in the oracle (a dropped scale, a transposed
+operand, a flipped or off-by-one mask, a wrong stride, a missing normalisation)
+fails at least one of them; ``test_oracle_mutants.py`` plants such slips in a copy
+of the oracle's C source and checks that.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+C, P = oracle.MASK_CAUSAL, oracle.MASK_KEY_PADDING
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _h(x):
+    """[n, d] -> [1, 1, n, d] float64."""
+    return np.asarray(x, np.float64)[None, None]
+
+
+def _rand(seed, B, H, n_q, n_k, d_k, d_v):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return (rng.standard_normal((B, H, n_q, d_k)), rng.standard_normal((B, H, n_k, d_k)),
+            rng.standard_normal((B, H, n_k, d_v)))
+
+
+# ---------------------------------------------------------------- worked examples
+def pin_two_token_printed(orc):
+    """attention-paper-guide section 03.2: the page's own printed numbers."""
+    g = _golden("two_token_example.json")
+    sc = 1.0 / math.sqrt(g["d_k"])
+    Q, K, V = _h(g["Q"]), _h(g["K"]), _h(g["V"])
+    out, _ = orc.attention(Q, K, V, sc)
+    w = orc.attention_weights(Q, K, sc)[0, 0]
+    pr, tol = g["printed"], g["tolerance_from_printing"]
+    assert np.allclose(np.asarray(g["Q"]) @ np.asarray(g["K"]).T, pr["scores_unscaled"])
+    assert np.abs(np.log(w[:, 1] / w[:, 0]) - (np.array(pr["scores_scaled"])[:, 1] - np.array(pr["scores_scaled"])[:, 0])).max() < 2 * tol["scores_scaled"]
+    assert np.abs(w - pr["weights"]).max() <= tol["weights"]
+    assert np.abs(out[0, 0] - pr["output"]).max() <= tol["output"]
+    assert np.abs(out[0, 0, 1] - pr["output_row1_in_text"]).max() <= tol["output_row1_in_text"]
+
+
+def pin_two_token_closed_form(orc):
+    """The same example solved by hand.
+
+    Scaled scores are [c, c] for query 0 and [0, c] for query 1 with c = 1/sqrt(2).
+    Query 0 therefore weights both keys 1/2: o_0 = (10/2, 6/2) = (5, 3) and
+    lse_0 = c + ln 2. Query 1 weights them 1/(1+e^c) and e^c/(1+e^c):
+    o_1 = (10/(1+e^c), 6 e^c/(1+e^c)) and lse_1 = ln(1 + e^c).
+    """
+    g = _golden("two_token_example.json")
+    c = 1.0 / math.sqrt(2.0)
+    out, lse = orc.attention(_h(g["Q"]), _h(g["K"]), _h(g["V"]), c)
+    e = math.exp(c)
+    want = np.array([[5.0, 3.0], [10.0 / (1.0 + e), 6.0 * e / (1.0 + e)]])
+    assert np.abs(out[0, 0] - want).max() < 1e-13
+    assert abs(lse[0, 0, 0] - (c + math.log(2.0))) < 1e-13
+    assert abs(lse[0, 0, 1] - math.log1p(e)) < 1e-13
+
+
+def pin_running_example_unmasked(orc):
+    """rockcohen.cc section 5.1 ledger: S, A and z_0 from the printed Q, K, V."""
+    g = _golden("running_example_4token.json")
+    sc = 1.0 / math.sqrt(g["d_k"])
+    Q, K, V = _h(g["Q"]), _h(g["K"]), _h(g["V"])
+    pr, tol = g["printed"], g["tolerance"]
+    assert abs(float(np.dot(g["Q"][0], g["K"][1])) - pr["q0_dot_k1_unscaled"]) <= tol["q0_dot_k1_unscaled"]
+    # one-key-at-a-time calls expose the scaled score itself: with a single legal
+    # key, lse = ln exp(s) = s
+    for j in range(4):
+        _, lse = orc.attention(Q, K[:, :, j:j + 1], V[:, :, j:j + 1], sc)
+        assert np.abs(lse[0, 0] - np.asarray(pr["S_scaled"])[:, j]).max() <= tol["S_scaled"]
+    w = orc.attention_weights(Q, K, sc)[0, 0]
+    assert np.abs(w - pr["A"]).max() <= tol["A"]
+    out, _ = orc.attention(Q, K, V, sc)
+    assert np.abs(out[0, 0, 0] - pr["z0"]).max() <= tol["z0"]
+
+
+def pin_running_example_causal(orc):
+    """rockcohen.cc sections 5.3 and 6.3: causal rows, exact zeros above the diagonal."""
+    g = _golden("running_example_4token.json")
+    sc = 1.0 / math.sqrt(g["d_k"])
+    Q, K, V = _h(g["Q"]), _h(g["K"]), _h(g["V"])
+    w = orc.attention_weights(Q, K, sc, C)[0, 0]
+    pr, tol = g["printed"], g["tolerance"]
+    assert np.array_equal(w[0], np.array(pr["causal_A_row0"], np.float64))
+    assert np.abs(w[1] - pr["causal_A_row1"]).max() <= tol["causal"]
+    assert np.all(w[np.triu_indices(4, 1)] == 0.0)
+    out, _ = orc.attention(Q, K, V, sc, C)
+    assert np.array_equal(out[0, 0, 0], np.asarray(g["V"], np.float64)[0])
+
+
+def pin_softmax_example(orc):
+    """rockcohen.cc section 3.2: softmax of (3.2, 0.1, -2.5, 0.4)."""
+    g = _golden("softmax_example.json")
+    q = np.ones((1, 1, 1, 1))
+    k = np.asarray(g["scores"], np.float64).reshape(1, 1, 4, 1)
+    out, _ = orc.attention(q, k, np.eye(4)[None, None], 1.0)
+    assert np.all(np.abs(out[0, 0, 0] - g["printed_weights"]) <= np.asarray(g["tolerance_from_printing"]))
+
+
+# ---------------------------------------------------------------- invariants
+def pin_rows_sum_to_one_and_exact_zeros(orc):
+    """rockcohen.cc section 10.2 (P0b, P0c): rows sum to 1; illegal weights are exactly 0.0."""
+    q, k, _ = _rand(11, 2, 2, 7, 9, 5, 3)
+    kl = np.array([4, 9], np.int32)
+    for mode in (0, C, P, C | P):
+        n_k = 7 if mode & C else 9
+        w = orc.attention_weights(q, k[:, :, :n_k], 0.4, mode, kl)
+        assert np.abs(w.sum(-1) - 1.0).max() < 1e-13
+        illegal = ~oracle.legal_mask(2, 7, n_k, mode, kl)
+        assert np.all(w[np.broadcast_to(illegal, w.shape)] == 0.0)
+        assert np.all(w[np.broadcast_to(~illegal, w.shape)] > 0.0)
+
+
+def pin_permutation_equivariance(orc):
+    """rockcohen.cc section 6.2: permuting query rows permutes the output rows; permuting
+    key/value rows jointly leaves the output unchanged (no mask)."""
+    q, k, v = _rand(12, 1, 2, 6, 8, 4, 5)
+    out, lse = orc.attention(q, k, v, 0.5)
+    pq = np.random.Generator(np.random.PCG64(1)).permutation(6)
+    pk = np.random.Generator(np.random.PCG64(2)).permutation(8)
+    out_q, lse_q = orc.attention(q[:, :, pq], k, v, 0.5)
+    assert np.abs(out_q - out[:, :, pq]).max() < 1e-13 and np.abs(lse_q - lse[:, :, pq]).max() < 1e-13
+    out_k, lse_k = orc.attention(q, k[:, :, pk], v[:, :, pk], 0.5)
+    assert np.abs(out_k - out).max() < 1e-13 and np.abs(lse_k - lse).max() < 1e-13
+
+
+def pin_shift_invariance(orc):
+    """rockcohen.cc section 3.2: adding one constant to every score of a row changes
+    nothing. K + 1 u^T adds q_i . u to row i, so O is unchanged and lse moves by
+    scale * q_i . u."""
+    q, k, v = _rand(13, 1, 1, 5, 6, 3, 2)
+    u = np.array([0.7, -1.3, 2.1])
+    out, lse = orc.attention(q, k, v, 0.6, P, np.array([4], np.int32))
+    out2, lse2 = orc.attention(q, k + u, v, 0.6, P, np.array([4], np.int32))
+    assert np.abs(out2 - out).max() < 1e-12
+    assert np.abs(lse2 - (lse + 0.6 * (q @ u))).max() < 1e-12
+
+
+def pin_zero_query_is_mean_of_legal_values(orc):
+    """Closed form: with Q = 0 every legal score is 0, so o_i is the plain mean of the
+    legal V rows (causal: rows 0..i; key padding: rows 0..len-1)."""
+    _, k, v = _rand(14, 2, 1, 5, 5, 3, 4)
+    q = np.zeros((2, 1, 5, 3))
+    kl = np.array([3, 5], np.int32)
+    out, lse = orc.attention(q, k, v, 0.5, C | P, kl)
+    for b in range(2):
+        for i in range(5):
+            n = min(i + 1, kl[b])
+            assert np.abs(out[b, 0, i] - v[b, 0, :n].mean(0)).max() < 1e-14
+            assert abs(lse[b, 0, i] - math.log(n)) < 1e-14
+
+
+def pin_causal_row_is_prefix_attention(orc):
+    """rockcohen.cc section 6.3: causal row i is attention over keys 0..i alone."""
+    q, k, v = _rand(15, 1, 1, 6, 6, 4, 3)
+    out, lse = orc.attention(q, k, v, 0.5, C)
+    for i in range(6):
+        o_i, l_i = orc.attention(q[:, :, i:i + 1], k[:, :, :i + 1], v[:, :, :i + 1], 0.5)
+        assert np.abs(out[0, 0, i] - o_i[0, 0, 0]).max() < 1e-13 and abs(lse[0, 0, i] - l_i[0, 0, 0]) < 1e-13
+
+
+def pin_key_padding_is_truncation(orc):
+    """Key padding with length L equals the unpadded call on the first L keys."""
+    q, k, v = _rand(16, 3, 2, 4, 9, 3, 5)
+    kl = np.array([1, 5, 9], np.int32)
+    out, lse = orc.attention(q, k, v, 0.3, P, kl)
+    for b, L in enumerate(kl):
+        o_b, l_b = orc.attention(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.3)
+        assert np.abs(out[b] - o_b[0]).max() < 1e-13 and np.abs(lse[b] - l_b[0]).max() < 1e-13
+    # one legal key: the output is that key's value row, exactly
+    assert np.array_equal(out[0, :, :, :], np.broadcast_to(v[0, :, :1, :], out[0].shape))
+
+
+def pin_heads_are_independent(orc):
+    """vlmlib.cn summary, multi-head attention: each (b, h) is its own attention call."""
+    q, k, v = _rand(17, 2, 3, 5, 7, 4, 6)
+    out, lse = orc.attention(q, k, v, 0.5)
+    for b in range(2):
+        for h in range(3):
+            o, l = orc.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], 0.5)
+            assert np.array_equal(o[0, 0], out[b, h]) and np.array_equal(l[0, 0], lse[b, h])
+
+
+def pin_loop_form_equals_matrix_form(orc):
+    """rockcohen.cc section 10.2 (P0a): loop form equals matrix form to 1e-12. The
+    matrix form uses numpy matmul and scipy's softmax / logsumexp (library steps),
+    across self and cross shapes, d_k != d_v, every mask mode and B*H > 1."""
+    for seed, (B, H, n_q, n_k, d_k, d_v) in enumerate([(2, 3, 5, 7, 4, 6), (1, 2, 9, 4, 8, 3), (3, 1, 6, 6, 2, 5)]):
+        q, k, v = _rand(100 + seed, B, H, n_q, n_k, d_k, d_v)
+        kl = np.random.Generator(np.random.PCG64(seed)).integers(1, n_k, B, endpoint=True).astype(np.int32)
+        for mode in (0, C, P, C | P):
+            if mode & C and n_q != n_k:
+                continue
+            out, lse = orc.attention(q, k, v, 0.37, mode, kl)
+            out_m, lse_m, A = oracle.attention_matrix_form(q, k, v, 0.37, mode, kl)
+            assert np.abs(out - out_m).max() < 1e-12 and np.abs(lse - lse_m).max() < 1e-12
+            w = orc.attention_weights(q, k, 0.37, mode, kl)
+            assert np.abs(w - A).max() < 1e-12
+
+
+def pin_torch_cpu_reference(orc):
+    """Library cross-check: torch float64 on the CPU, softmax(scale QK^T + mask) V."""
+    import torch
+
+    q, k, v = _rand(18, 2, 2, 6, 6, 5, 3)
+    kl = np.array([6, 3], np.int32)
+    for mode in (0, C, P, C | P):
+        mask = torch.from_numpy(np.where(oracle.legal_mask(2, 6, 6, mode, kl), 0.0, -np.inf))
+        s = 0.45 * torch.from_numpy(q) @ torch.from_numpy(k).transpose(-1, -2) + mask
+        ref = torch.softmax(s, dim=-1) @ torch.from_numpy(v)
+        out, lse = orc.attention(q, k, v, 0.45, mode, kl)
+        assert np.abs(out - ref.numpy()).max() < 1e-12
+        assert np.abs(lse - torch.logsumexp(s, dim=-1).numpy()).max() < 1e-12
+
+
+def pin_brute_force_tiny(orc):
+    """Pure-Python brute force with math.exp, tiny cross-attention shape with padding."""
+    q, k, v = _rand(19, 1, 1, 3, 4, 2, 3)
+    L = 3
+    out, lse = orc.attention(q, k, v, 0.8, P, np.array([L], np.int32))
+    for i in range(3):
+        e = [math.exp(0.8 * sum(q[0, 0, i, t] * k[0, 0, j, t] for t in range(2))) for j in range(L)]
+        tot = sum(e)
+        for t in range(3):
+            assert abs(out[0, 0, i, t] - sum(e[j] * v[0, 0, j, t] for j in range(L)) / tot) < 1e-13
+        assert abs(lse[0, 0, i] - math.log(tot)) < 1e-13
+
+
+def pin_empty_row_convention(orc):
+    """No legal key (key length 0): the chosen convention o = 0, lse = -inf."""
+    q, k, v = _rand(20, 2, 1, 3, 4, 2, 2)
+    out, lse = orc.attention(q, k, v, 0.5, P, np.array([0, 2], np.int32))
+    assert np.all(out[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(lse[1]))
+
+
+def pin_row_subset_matches_full(orc):
+    """attention_rows returns exactly the rows of the full call."""
+    q, k, v = _rand(21, 2, 2, 5, 6, 3, 4)
+    kl = np.array([2, 6], np.int32)
+    out, lse = orc.attention(q, k, v, 0.5, P, kl)
+    ids = np.array([0, 7, 3, 19, 12])
+    o_r, l_r = orc.attention_rows(q, k, v, 0.5, ids, P, kl)
+    assert np.array_equal(o_r, out.reshape(-1, 4)[ids]) and np.array_equal(l_r, lse.reshape(-1)[ids])
+
+
+def pin_input_widening(orc):
+    """bf16 bit patterns and float32 inputs are widened exactly: same result as float64
+    inputs holding the same values."""
+    q, k, v = _rand(22, 1, 2, 4, 5, 3, 3)
+    f32 = [a.astype(np.float32) for a in (q, k, v)]
+    bits = [(a.view(np.uint32) >> 16).astype(np.uint16) for a in f32]  # truncation: any bf16 values will do
+    for arrs in (f32, bits):
+        o1, l1 = orc.attention(*arrs, 0.5)
+        o2, l2 = orc.attention(*[oracle.widen(a) for a in arrs], 0.5)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # bf16 1.0 is 0x3F80, -2.0 is 0xC000
+    assert np.array_equal(oracle.widen(np.array([0x3F80, 0xC000], np.uint16)), [1.0, -2.0])
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,72 @@
+"""Planted mistakes in a copy of the oracle must fail at least one pin (no GPU).
+
+Each mutant is a one-line edit of ``oracle/attn_oracle.c`` of the kind a careful
+author could still make: a dropped scale, a transposed operand, a flipped or
+off-by-one mask, a wrong stride or head offset, a missing normalisation or log.
+It is compiled into a temporary directory and the pins of ``oracle_pins.py`` run
+against it in a child process (so an out-of-range read in a mutant cannot take
+the test runner down). The real oracle source is never modified.
+"""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+import oracle
+
+MUTANTS = {
+    "scale_dropped": ("s[j] = p->scale * dot;", "s[j] = dot;"),
+    "k_transposed": ("koff + (long long)j * p->d_k + t", "koff + (long long)t * p->n_k + j"),
+    "causal_flipped": ("&& j > i) return 0;", "&& j < i) return 0;"),
+    "causal_off_by_one": ("&& j > i) return 0;", "&& j >= i) return 0;"),
+    "padding_off_by_one": ("j >= p->key_lens[b]", "j > p->key_lens[b]"),
+    "padding_wrong_batch": ("int b = bh / p->H;", "int b = bh % p->B;"),
+    "mask_ignored": ("if (!legal(p, b, i, j)) {", "if (0) {"),
+    "exp_sign": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
+    "not_normalised": ("s[j] = s[j] / l;", "s[j] = s[j];"),
+    "lse_missing_log": ("? m + log(l) :", "? m + l :"),
+    "v_row_stride": ("voff + (long long)j * p->d_v + t", "voff + (long long)j * p->d_k + t"),
+    "k_head_offset": ("long long koff = (long long)bh * p->n_k * p->d_k;",
+                      "long long koff = (long long)(bh / p->H) * p->n_k * p->d_k;"),
+    "v_head_offset": ("long long voff = (long long)bh * p->n_k * p->d_v;",
+                      "long long voff = (long long)(bh / p->H) * p->n_k * p->d_v;"),
+    "q_row_reversed": ("((long long)bh * p->n_q + i) * p->d_k", "((long long)bh * p->n_q + (p->n_q - 1 - i)) * p->d_k"),
+    "bf16_widening": ("<< 16;", "<< 15;"),
+}
+
+_CHILD = r"""
+import sys
+sys.path[:0] = [{root!r}, {tests!r}]
+import oracle
+from oracle_pins import PINS
+orc = oracle.Oracle({lib!r})
+failed = []
+for pin in PINS:
+    try:
+        pin(orc)
+    except Exception as e:
+        failed.append(pin.__name__)
+print("FAILED:" + ",".join(failed))
+"""
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    with open(oracle.SRC) as f:
+        src = f.read()
+    before, after = MUTANTS[name]
+    assert src.count(before) == 1, f"mutation site for {name!r} not found exactly once in the oracle source"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    tests = os.path.dirname(os.path.abspath(__file__))
+    with tempfile.TemporaryDirectory() as tmp:
+        src_path = os.path.join(tmp, "attn_oracle.c")
+        with open(src_path, "w") as f:
+            f.write(src.replace(before, after))
+        lib = oracle.build(src_path, os.path.join(tmp, "liboracle_mutant.so"))
+        code = _CHILD.format(root=root, tests=tests, lib=lib)
+        res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    caught = [ln for ln in res.stdout.splitlines() if ln.startswith("FAILED:")]
+    # a crash of the child also counts as caught; a clean run with no failed pin does not
+    assert res.returncode != 0 or (caught and caught[-1] != "FAILED:"), f"mutant {name!r} passed every pin"

@@ -1,0 +1,130 @@
+"""Seeded synthetic inputs for attention workloads.
+
+This module holds no attention arithmetic: it only names the workload shapes and
+draws their inputs, so both the CUDA path and the fp64 oracle are fed from it.
+
+Recipe (the same for every workload):
+  * generator: numpy PCG64 seeded with ``20170612 + index`` of the workload;
+  * Q, K, V: standard normal float32 draws in that order, times ``input_scale``;
+    bf16 workloads round them to bf16 with round-to-nearest-even (bit patterns
+    kept as uint16); float32 workloads keep them as drawn;
+  * key lengths (key-padding workloads only): integers drawn uniformly from the
+    inclusive range ``key_len_range`` after V.
+
+Shapes follow the pages' base and big Transformer sizes (d_model 512 with h = 8,
+d_model 1024 with h = 16, so d_k = d_v = 64 per head; vlmlib.cn summary,
+"multi-head attention"; transformer_lab, section 04) and the three uses of
+attention (rockcohen.cc, section 5.3).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+import math
+
+import numpy as np
+
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+SEED_BASE = 20170612
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    n_q: int
+    n_k: int
+    d_k: int
+    d_v: int
+    dtype: str  # "f32" or "bf16"
+    mask_mode: int
+    key_len_range: tuple | None = None
+    input_scale: float = 1.0
+    index: int = 0
+
+    @property
+    def seed(self) -> int:
+        return SEED_BASE + self.index
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(d_k), computed in double and rounded to float32."""
+        return default_scale(self.d_k)
+
+    def legal_pairs(self, key_lens=None) -> int:
+        """Number of legal (query, key) pairs over all heads."""
+        return legal_pairs(self.B, self.H, self.n_q, self.n_k, self.mask_mode, key_lens)
+
+    def algorithmic_flops(self, key_lens=None) -> float:
+        """2 (d_k + d_v) multiply-adds per legal pair: one QK^T dot and one P.V row."""
+        return 2.0 * (self.d_k + self.d_v) * self.legal_pairs(key_lens)
+
+    def dense_flops(self) -> float:
+        return 2.0 * (self.d_k + self.d_v) * self.B * self.H * self.n_q * self.n_k
+
+
+def default_scale(d_k: int) -> float:
+    return float(np.float32(1.0 / math.sqrt(d_k)))
+
+
+def legal_pairs(B, H, n_q, n_k, mask_mode, key_lens=None) -> int:
+    total = 0
+    for b in range(B):
+        lim = n_k
+        if mask_mode & MASK_KEY_PADDING:
+            lim = min(lim, int(key_lens[b]))
+        if mask_mode & MASK_CAUSAL:
+            # query i sees keys 0..min(i, lim-1)
+            full = min(n_q, lim)  # rows whose causal limit i+1 <= lim
+            total += full * (full + 1) // 2 + max(0, n_q - full) * lim
+        else:
+            total += n_q * lim
+    return total * H
+
+
+def _wl(index, name, B, H, n_q, n_k, d, dtype, mask, lens=None, scale=1.0):
+    return Workload(name, B, H, n_q, n_k, d, d, dtype, mask, lens, scale, index)
+
+
+WORKLOADS = {w.name: w for w in [
+    _wl(0, "tiny_f32_b1_h1_n16_d8", 1, 1, 16, 16, 8, "f32", MASK_NONE),
+    _wl(1, "encoder_self_pad_b32_h8_n128_d64", 32, 8, 128, 128, 64, "bf16", MASK_KEY_PADDING, (64, 128)),
+    _wl(2, "decoder_causal_b16_h8_n512_d64", 16, 8, 512, 512, 64, "bf16", MASK_CAUSAL),
+    _wl(3, "cross_pad_b16_h16_q256_k512_d64", 16, 16, 256, 512, 64, "bf16", MASK_KEY_PADDING, (384, 512)),
+    _wl(4, "long_causal_b2_h16_n8192_d64", 2, 16, 8192, 8192, 64, "bf16", MASK_CAUSAL, None, 0.5),
+    _wl(5, "long_none_b2_h16_n8192_d64", 2, 16, 8192, 8192, 64, "bf16", MASK_NONE, None, 0.5),
+    _wl(6, "long_causal_b2_h16_n8192_d128", 2, 16, 8192, 8192, 128, "bf16", MASK_CAUSAL, None, 0.5),
+    _wl(7, "long_none_b2_h16_n8192_d128", 2, 16, 8192, 8192, 128, "bf16", MASK_NONE, None, 0.5),
+]}
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def make_inputs(w: Workload, seed: int | None = None, **shape):
+    """Draw (q, k, v, key_lens) for a workload.
+
+    ``shape`` may override B, H, n_q, n_k, d_k, d_v (for reduced parity cases of
+    the same recipe). Returns numpy arrays: uint16 bf16 bits or float32, and an
+    int32 ``key_lens`` of shape [B] (all n_k when the workload has no padding).
+    """
+    B, H = shape.get("B", w.B), shape.get("H", w.H)
+    n_q, n_k = shape.get("n_q", w.n_q), shape.get("n_k", w.n_k)
+    d_k, d_v = shape.get("d_k", w.d_k), shape.get("d_v", w.d_v)
+    rng = np.random.Generator(np.random.PCG64(w.seed if seed is None else seed))
+    arrs = []
+    for shp in ((B, H, n_q, d_k), (B, H, n_k, d_k), (B, H, n_k, d_v)):
+        x = rng.standard_normal(shp, dtype=np.float32)
+        if w.input_scale != 1.0:
+            x *= np.float32(w.input_scale)
+        arrs.append(to_bf16_bits(x) if w.dtype == "bf16" else x)
+    if w.mask_mode & MASK_KEY_PADDING:
+        lo, hi = w.key_len_range
+        lo, hi = min(lo, n_k), min(hi, n_k)
+        key_lens = rng.integers(lo, hi, size=B, endpoint=True).astype(np.int32)
+    else:
+        key_lens = np.full((B,), n_k, np.int32)
+    return arrs[0], arrs[1], arrs[2], key_lens
