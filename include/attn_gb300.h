@@ -1,0 +1,106 @@
+/*
+ * attn_gb300.h -- C ABI of the GB300 (sm_103a) scaled dot-product attention
+ * forward library, libattn_gb300.so.
+ *
+ * The operation (per batch b, head h, query row i):
+ *
+ *   O[b,h,i,:] = sum_j softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] + mask(b,i,j) ) V[b,h,j,:]
+ *
+ * i.e. Eq. (1), Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V, of "Attention
+ * Is All You Need" (rockcohen.cc/paper/t1-transformer, section 5.1; vlmlib.cn
+ * paper summary, "scaled dot-product attention"), applied independently to
+ * every head of multi-head attention (vlmlib.cn, "multi-head attention";
+ * rockcohen.cc section 5.2). mask(b,i,j) is 0 for a legal connection and -inf for
+ * an illegal one, added at the softmax input, so illegal keys get an exact zero
+ * weight (rockcohen.cc sections 5.3 and 6.3). The three uses of attention
+ * (rockcohen.cc section 5.3) are expressed through mask_mode and the shapes:
+ *   encoder self-attention      ATTN_MASK_KEY_PADDING, n_q == n_k
+ *   decoder masked self-attn.   ATTN_MASK_CAUSAL (optionally | KEY_PADDING), n_q == n_k
+ *   encoder-decoder attention   ATTN_MASK_KEY_PADDING or NONE, n_q != n_k allowed
+ *
+ * Conventions shared by the entry points below:
+ *   - Layouts are contiguous row-major [B, h, n, d] (the per-head layout that a
+ *     split_heads reshape produces, csdn blog reimplementation):
+ *       q   [B, h, n_q, d_k]    k [B, h, n_k, d_k]    v [B, h, n_k, d_v]
+ *       out [B, h, n_q, d_v]    lse [B, h, n_q] (float32, optional)
+ *   - Every pointer is a DEVICE pointer owned by the caller. The library
+ *     allocates no device memory; it neither keeps nor frees the pointers.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL
+ *     for the legacy default stream) and return before the GPU work finishes.
+ *   - scale is used exactly as given; callers normally pass 1/sqrt(d_k) computed
+ *     in double and rounded to float.
+ *   - key_lens (int32 [B], device memory) gives each batch's number of valid keys
+ *     (right padding); key j of batch b is illegal when j >= key_lens[b]. It is
+ *     read only when mask_mode has ATTN_MASK_KEY_PADDING and may be NULL otherwise.
+ *     Values are clamped to [0, n_k].
+ *   - With ATTN_MASK_CAUSAL, key j is illegal for query i when j > i; it requires
+ *     n_q == n_k.
+ *   - lse[b,h,i] = ln sum_{j legal} exp(scale * q_i . k_j). A query row with no
+ *     legal key (key length 0) gets out = 0 and lse = -inf. lse may be NULL.
+ *   - Errors are returned as a status; nothing is printed and the process never
+ *     exits. A status other than ATTN_OK means nothing was launched.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID = -1,     /* null pointer, non-positive size, non-finite scale, bad mask,
+                                causal with n_q != n_k, misaligned pointer, size overflow */
+  ATTN_ERR_UNSUPPORTED = -2, /* shape this path does not implement (see each entry point) */
+  ATTN_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed (no GPU, launch error, ...) */
+  ATTN_ERR_TIMEOUT = -4      /* a kernel gave up waiting on an internal barrier (reported by
+                                attn_fault_status) */
+} attn_status;
+
+enum { ATTN_MASK_NONE = 0, ATTN_MASK_CAUSAL = 1, ATTN_MASK_KEY_PADDING = 2 };
+
+/*
+ * attn_fwd -- bf16 inputs and output, fp32 accumulation (sm_103a tensor cores).
+ *   q, k, v, out: bf16 (raw 16-bit) arrays, 16-byte aligned.
+ *   lse: float32 or NULL.
+ *   Supported: d_k == d_v in {64, 128}; any B, h, n_q, n_k >= 1 whose element
+ *   counts fit in int32 per head-row index and whose byte strides fit TMA limits.
+ *   Otherwise ATTN_ERR_UNSUPPORTED.
+ * Numerics: QK^T and PV accumulate in fp32 on the tensor cores; the softmax is the
+ * online (running max / running sum) form in fp32 with exp2 and the scale folded
+ * in; the probabilities are rounded to bf16 before the PV product; the output is
+ * divided by the row sum in fp32 and rounded to bf16 (nearest-even).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+             int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
+             int mask_mode, const int32_t* key_lens, void* stream);
+
+/*
+ * attn_fwd_f32 -- float32 inputs and output, float32 arithmetic throughout
+ * (CUDA cores). Same semantics and conventions as attn_fwd; pointers 4-byte
+ * aligned; 1 <= d_k, d_v <= 256, otherwise ATTN_ERR_UNSUPPORTED.
+ */
+int attn_fwd_f32(const float* q, const float* k, const float* v, float* out, float* lse,
+                 int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
+                 int mask_mode, const int32_t* key_lens, void* stream);
+
+/*
+ * attn_fault_status -- synchronises `stream`, then reports whether any kernel of
+ * this library on the current device gave up waiting on one of its internal
+ * barriers since the last clear (each such wait is bounded in time; a kernel that
+ * gives up writes no further output and returns). Returns ATTN_OK,
+ * ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA. If `clear` is non-zero the record is reset.
+ * `fault_code` (may be NULL) receives the raw record: bit 0 producer, bit 1 MMA
+ * issuer, bit 2 softmax, bit 3 epilogue.
+ */
+int attn_fault_status(void* stream, int clear, uint32_t* fault_code);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char* attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTN_GB300_H */

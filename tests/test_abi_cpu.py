@@ -1,0 +1,94 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, and rejects
+bad arguments with the documented status codes -- all without a GPU (argument
+validation returns before any CUDA call)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from transformer_scaled_dot_mha_gb300 import attn, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return attn.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    assert {"attn_fwd", "attn_fwd_f32", "attn_fault_status", "attn_status_string"} <= set(declared_functions())
+
+
+def test_every_declared_symbol_is_exported(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", attn.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = {ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_status_strings(L):
+    for st in (0, -1, -2, -3, -4):
+        assert attn.status_string(st).startswith("ATTN_")
+    assert "unknown" in attn.status_string(12345)
+
+
+VALID = dict(q=16, k=32, v=48, out=64, lse=None, B=1, h=1, n_q=8, n_k=8, d_k=64, d_v=64, scale=0.125,
+             mask_mode=0, key_lens=None)
+
+
+def call(L, fn="attn_fwd", **kw):
+    a = dict(VALID, **kw)
+    return getattr(L, fn)(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["h"], a["n_q"], a["n_k"], a["d_k"],
+                          a["d_v"], a["scale"], a["mask_mode"], a["key_lens"], None)
+
+
+@pytest.mark.parametrize("fn", ["attn_fwd", "attn_fwd_f32"])
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(k=None), dict(v=None), dict(out=None),
+    dict(B=0), dict(h=-1), dict(n_q=0), dict(n_k=0), dict(d_k=0), dict(d_v=0),
+    dict(scale=float("inf")), dict(scale=float("nan")),
+    dict(mask_mode=4), dict(mask_mode=-1),
+    dict(mask_mode=1, n_k=9),                     # causal needs n_q == n_k
+    dict(mask_mode=2, key_lens=None),             # key padding needs key_lens
+    dict(mask_mode=2, key_lens=2),                # misaligned key_lens
+    dict(lse=6),                                  # misaligned lse
+    dict(B=1 << 16, h=1 << 16),                   # B*h overflows int32
+])
+def test_invalid_arguments(L, fn, bad):
+    assert call(L, fn, **bad) == attn.ATTN_ERR_INVALID
+
+
+def test_bf16_alignment_and_unsupported_shapes(L):
+    assert call(L, q=8) == attn.ATTN_ERR_INVALID          # bf16 path needs 16-byte alignment
+    assert call(L, out=72) == attn.ATTN_ERR_INVALID
+    assert call(L, d_k=32, d_v=32) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(L, d_k=64, d_v=128) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(L, d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(L, "attn_fwd_f32", d_k=257) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(L, "attn_fwd_f32", q=18) == attn.ATTN_ERR_INVALID
+
+
+def test_library_has_no_oracle_dependency():
+    """The product library never links or names the oracle."""
+    build.build()
+    out = subprocess.run(["nm", "-D", attn.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    assert "oracle" not in out
+    deps = subprocess.run(["readelf", "-d", attn.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    assert "liboracle" not in deps
+    for src in glob.glob(os.path.join(ROOT, "transformer_scaled_dot_mha_gb300", "**", "*.*"), recursive=True):
+        if src.endswith((".py", ".cu", ".cuh", ".h")):
+            assert "import oracle" not in open(src).read() and "attn_oracle" not in open(src).read(), src

@@ -1,0 +1,119 @@
+"""Python binding of libattn_gb300.so: the C entry points of include/attn_gb300.h
+under the same names, plus tensor-shaped wrappers.
+
+This module only marshals arguments (tensor shapes, data pointers, the current
+CUDA stream) and turns status codes into exceptions; every step of the
+attention computation runs in the library's kernels. There is no fallback: if
+the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gb300.so")
+
+ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 0, -1, -2, -3, -4
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (loaded once)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
+        L.attn_fwd.restype = i
+        L.attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
+        L.attn_fwd_f32.restype = i
+        L.attn_fault_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint32)]
+        L.attn_fault_status.restype = i
+        L.attn_status_string.argtypes = [i]
+        L.attn_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, dtype, ndim=4):
+    if t.dtype != dtype or t.dim() != ndim or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D CUDA {dtype} tensor, got {t.dtype} {tuple(t.shape)}")
+
+
+def _call(fn, q, k, v, out, lse, scale, mask_mode, key_lens, stream, dtype, where):
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check(t, n, dtype)
+    B, H, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    if k.shape != (B, H, n_k, d_k) or v.shape != (B, H, n_k, d_v) or out.shape != (B, H, n_q, d_v):
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)} out{tuple(out.shape)}")
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 3)
+        if lse.shape != (B, H, n_q):
+            raise ValueError("lse must have shape [B, H, n_q]")
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, 1)
+        if key_lens.shape != (B,):
+            raise ValueError("key_lens must have shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, n_q, n_k, d_k, d_v, float(scale), int(mask_mode),
+            _ptr(key_lens), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, where)
+    return out
+
+
+def attn_fwd(q, k, v, out, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
+    """bf16 forward into caller-provided ``out`` (and optional fp32 ``lse``)."""
+    return _call(lib().attn_fwd, q, k, v, out, lse, scale, mask_mode, key_lens, stream, torch.bfloat16, "attn_fwd")
+
+
+def attn_fwd_f32(q, k, v, out, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
+    """float32 forward into caller-provided ``out`` (and optional ``lse``)."""
+    return _call(lib().attn_fwd_f32, q, k, v, out, lse, scale, mask_mode, key_lens, stream, torch.float32,
+                 "attn_fwd_f32")
+
+
+def attention(q, k, v, scale=None, mask_mode=MASK_NONE, key_lens=None, with_lse=False, stream=None):
+    """Allocating convenience wrapper: returns ``out`` (and ``lse``) for bf16 or float32 inputs."""
+    B, H, n_q, _ = q.shape
+    out = torch.empty((B, H, n_q, v.shape[3]), dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device) if with_lse else None
+    fn = attn_fwd if q.dtype == torch.bfloat16 else attn_fwd_f32
+    fn(q, k, v, out, lse, scale, mask_mode, key_lens, stream)
+    return (out, lse) if with_lse else out
+
+
+def attn_fault_status(stream=None, clear=True):
+    """(status, raw fault bits) after synchronising ``stream``."""
+    code = ctypes.c_uint32(0)
+    st = lib().attn_fault_status(_stream_handle(stream), int(clear), ctypes.byref(code))
+    return st, code.value

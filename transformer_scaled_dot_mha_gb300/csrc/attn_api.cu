@@ -1,0 +1,90 @@
+// attn_api.cu -- the extern "C" entry points of libattn_gb300.so: argument
+// validation, the tensor-map encoder lookup, and dispatch to the kernels. The
+// semantics are documented in include/attn_gb300.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+
+namespace {
+
+attn::PFN_encodeTiled tensor_map_encoder() {
+  static attn::PFN_encodeTiled fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult qres = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qres) !=
+            cudaSuccess ||
+        qres != cudaDriverEntryPointSuccess)
+      return static_cast<attn::PFN_encodeTiled>(nullptr);
+    return reinterpret_cast<attn::PFN_encodeTiled>(f);
+  }();
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Checks shared by both entry points; returns ATTN_OK or an error status.
+int check_common(const void* q, const void* k, const void* v, const void* out, const float* lse, int B, int h,
+                 int n_q, int n_k, int d_k, int d_v, float scale, int mask_mode, const int32_t* key_lens) {
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID;
+  if (B <= 0 || h <= 0 || n_q <= 0 || n_k <= 0 || d_k <= 0 || d_v <= 0) return ATTN_ERR_INVALID;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID;
+  if (mask_mode < 0 || mask_mode > (ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return ATTN_ERR_INVALID;
+  if ((mask_mode & ATTN_MASK_CAUSAL) && n_q != n_k) return ATTN_ERR_INVALID;
+  if ((mask_mode & ATTN_MASK_KEY_PADDING) && (!key_lens || !aligned(key_lens, 4))) return ATTN_ERR_INVALID;
+  if (lse && !aligned(lse, 4)) return ATTN_ERR_INVALID;
+  const long long bh = (long long)B * h;
+  if (bh > 0x7fffffffLL) return ATTN_ERR_INVALID;
+  // every element index must fit in a signed 64-bit offset with room to spare
+  const long long maxn = n_q > n_k ? n_q : n_k, maxd = d_k > d_v ? d_k : d_v;
+  if (bh * maxn > (1LL << 40) / maxd) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int h, int n_q, int n_k,
+             int d_k, int d_v, float scale, int mask_mode, const int32_t* key_lens, void* stream) {
+  int st = check_common(q, k, v, out, lse, B, h, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::TcArgs a{q, k, v, out, lse, B, h, n_q, n_k, d_k, scale, mask_mode, key_lens,
+                 static_cast<cudaStream_t>(stream)};
+  return attn::launch_attn_tc(a, enc);
+}
+
+int attn_fwd_f32(const float* q, const float* k, const float* v, float* out, float* lse, int B, int h, int n_q,
+                 int n_k, int d_k, int d_v, float scale, int mask_mode, const int32_t* key_lens, void* stream) {
+  int st = check_common(q, k, v, out, lse, B, h, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return ATTN_ERR_INVALID;
+  if (d_k > 256 || d_v > 256) return ATTN_ERR_UNSUPPORTED;
+  attn::F32Args a{q, k, v, out, lse, B, h, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens,
+                  static_cast<cudaStream_t>(stream)};
+  return attn::launch_attn_f32(a);
+}
+
+int attn_fault_status(void* stream, int clear, uint32_t* fault_code) {
+  return attn::read_fault_word(static_cast<cudaStream_t>(stream), clear, fault_code);
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID: return "ATTN_ERR_INVALID: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: shape not supported by this path";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call failed";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel gave up waiting on an internal barrier";
+    default: return "unknown attn status";
+  }
+}
+
+}  // extern "C"

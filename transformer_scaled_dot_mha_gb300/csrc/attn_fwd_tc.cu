@@ -1,0 +1,499 @@
+// attn_fwd_tc.cu -- bf16 scaled dot-product attention forward on the sm_103a
+// tensor cores (TMA + tcgen05 + TMEM), one fused kernel.
+//
+// What it computes is Eq. (1) of "Attention Is All You Need",
+// softmax(Q K^T / sqrt(d_k)) V, per (batch, head) (rockcohen.cc section 5.1;
+// vlmlib.cn summary, "scaled dot-product attention" and "multi-head attention"),
+// with illegal connections set to -inf at the softmax input (rockcohen.cc
+// sections 5.3 and 6.3). The softmax is evaluated tile by tile with a running
+// maximum and running sum -- the memory-access change that rockcohen.cc
+// section 6.1 notes leaves the mathematics unchanged -- so the n x n score
+// matrix never leaves the SM.
+//
+// Work decomposition. One CTA owns 256 query rows of one (b, h): two 128-row Q
+// tiles. It streams 128-key K/V tiles through a shared-memory ring filled by TMA.
+// Warp roles (384 threads = three warpgroups):
+//   warps 0-3  softmax warpgroup for Q tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax warpgroup for Q tile 1
+//   warp  8    TMA producer (one lane)
+//   warp  9    MMA issuer (one lane); also allocates / frees TMEM
+//   warps 10-11 idle members of the control warpgroup
+// The control warpgroup hands registers to the softmax warpgroups (setmaxnreg:
+// 56 and 224 per thread; 128*56 + 256*224 = 384*168, the launch allocation).
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   [0,128)   S0 = Q0 K_j^T (fp32); P0 (bf16 pairs) overwrites its first 64 columns
+//   [128,256) S1 / P1
+//   [256, 256+D) O0 accumulator, [256+D, 256+2D) O1 accumulator (fp32)
+// Per K/V tile j the MMA issuer runs, in order,
+//   PV0(j-1): O0 += P0 V_{j-1};  S0(j) = Q0 K_j^T;  PV1(j-1);  S1(j)
+// so each softmax warpgroup works while the tensor core serves the other tile.
+// The softmax rescales O only when a row maximum grows by more than 2^8 (a lazy
+// reference maximum); the final O / l is exact whatever reference was used.
+//
+// Every wait on an mbarrier is bounded in time. A wait that runs out records a
+// fault bit (attn_fault_status), raises a CTA-wide abort flag, and every role then
+// stops, waits (bounded) for its own TMA copies or MMAs in flight, frees TMEM and
+// returns. Nothing traps.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace attn {
+
+__device__ unsigned int g_fault_word;  // fault record read by attn_fault_status
+
+namespace {
+
+constexpr int BM = 128;  // query rows per Q tile (= TMEM lanes)
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int THREADS = 384;
+constexpr int REGS_CONTROL = 56;
+constexpr int REGS_SOFTMAX = 224;
+constexpr int WARP_LOAD = 8;
+constexpr int WARP_MMA = 9;
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain copies in flight
+constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when max grows > 2^8
+
+constexpr uint32_t FAULT_PRODUCER = 1, FAULT_MMA = 2, FAULT_SOFTMAX = 4, FAULT_EPILOGUE = 8;
+
+template <int D>
+struct Cfg {
+  static constexpr int CHUNKS = D / 64;           // 128-byte swizzle atoms per row
+  static constexpr int CHUNK_BYTES = BM * 128;    // one 128-row x 64-column slab
+  static constexpr int TILE_BYTES = BM * D * 2;   // one 128-row tile of Q, K or V
+  static constexpr int STAGES = (D == 64) ? 4 : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+  // barrier indices
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_KEMPTY = B_KFULL + STAGES;
+  static constexpr int B_VFULL = B_KEMPTY + STAGES;
+  static constexpr int B_VEMPTY = B_VFULL + STAGES;
+  static constexpr int B_SFULL = B_VEMPTY + STAGES;  // [2]
+  static constexpr int B_PFULL = B_SFULL + 2;        // [2]
+  static constexpr int B_ODONE = B_PFULL + 2;        // [2]
+  static constexpr int B_DRAIN = B_ODONE + 2;
+  static constexpr int NUM_BARS = B_DRAIN + 1;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+  static constexpr int SMEM_USED = OFF_ABORT + 4;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TMEM_O = 2 * BN;
+  static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);  // Q, K both K-major
+  static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);   // V is MN-major
+  static_assert(TMEM_O + 2 * D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct Params {
+  uint16_t* out;
+  float* lse;
+  const int32_t* key_lens;
+  int H, n_q, n_k, mask_mode;
+  int BH, num_qblocks;
+  float scale_log2;  // scale * log2(e)
+};
+
+// Bounded wait on an mbarrier phase. Returns false (after recording `who`) if the
+// phase did not complete within kWaitLimitNs, or if another role already aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t who) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(&g_fault_word, who);
+        return false;
+      }
+    }
+  }
+}
+
+// Used only while tearing down after an abort: wait a short time, no side effects.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) return;
+}
+
+// Number of K/V tiles Q tile t (rows [r0, r0+128)) must visit.
+__device__ __forceinline__ int tiles_for(int r0, int n_q, int kv_tiles, bool causal) {
+  if (r0 >= n_q) return 0;
+  return causal ? min(kv_tiles, r0 / BN + 1) : kv_tiles;
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = ptx::smem_u32(smem);
+  const uint32_t s_q = s_base + C::OFF_Q, s_k = s_base + C::OFF_K, s_v = s_base + C::OFF_V;
+  auto bar = [&](int i) -> uint32_t { return s_base + C::OFF_BAR + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- which 256 query rows of which (b, h): heaviest causal blocks first
+  const int bh = blockIdx.x % p.BH;
+  const int qb = p.num_qblocks - 1 - blockIdx.x / p.BH;
+  const int b = bh / p.H;
+  const int row0 = qb * 2 * BM;
+  const bool causal = (p.mask_mode & 1) != 0;
+  int kv_len = p.n_k;
+  if (p.mask_mode & 2) kv_len = min(max(p.key_lens[b], 0), p.n_k);
+  const int kv_tiles = (kv_len + BN - 1) / BN;
+  const int n_t0 = tiles_for(row0, p.n_q, kv_tiles, causal);
+  const int n_t1 = tiles_for(row0 + BM, p.n_q, kv_tiles, causal);
+  const int n_max = max(n_t0, n_t1);
+
+  // ---- set-up: barriers, TMEM
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(C::B_QFULL), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(bar(C::B_KFULL + s), 1);
+      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);
+      ptx::mbar_init(bar(C::B_VFULL + s), 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(bar(C::B_SFULL + t), 1);
+      ptx::mbar_init(bar(C::B_PFULL + t), BM);  // every softmax thread arrives
+      ptx::mbar_init(bar(C::B_ODONE + t), 1);
+    }
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == WARP_LOAD && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CONTROL));
+    if (warp == WARP_LOAD) {
+    // ================================================================ producer
+    if (lane == 0 && n_max > 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      const int n_qt = (n_t1 > 0) ? 2 : 1;
+      ptx::mbar_arrive_expect_tx(bar(C::B_QFULL), n_qt * C::TILE_BYTES);
+      for (int t = 0; t < n_qt; ++t)
+        for (int c = 0; c < C::CHUNKS; ++c)
+          ptx::tma_load_3d(s_q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL), c * 64,
+                           row0 + t * BM, bh, pol_q);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_max && ok; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        ok = wait_bar(bar(C::B_KEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
+        for (int c = 0; c < C::CHUNKS; ++c)
+          ptx::tma_load_3d(s_k + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + s), c * 64, j * BN,
+                           bh, pol_kv);
+        ok = wait_bar(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER);
+        if (!ok) {
+          issued = 2 * j + 1;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
+        for (int c = 0; c < C::CHUNKS; ++c)
+          ptx::tma_load_3d(s_v + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bar(C::B_VFULL + s), c * 64, j * BN,
+                           bh, pol_kv);
+        issued = 2 * j + 2;
+      }
+      if (!ok) {
+        // copies still in flight must land before this CTA's shared memory goes away
+        drain_wait(bar(C::B_QFULL), 0);
+        for (int x = max(0, issued - 2 * C::STAGES); x < issued; ++x) {
+          const int j = x >> 1, s = j % C::STAGES;
+          const uint32_t ph = (j / C::STAGES) & 1;
+          drain_wait(bar(((x & 1) ? C::B_VFULL : C::B_KFULL) + s), ph);
+        }
+      }
+    }
+    __syncwarp();
+    } else if (warp == WARP_MMA) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && n_max > 0) {
+      const int n_t[2] = {n_t0, n_t1};
+      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
+      ptx::tc_fence_after();
+      for (int j = 0; j <= n_max && ok; ++j) {
+        if (j < n_max) {
+          ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          if (!ok) break;
+        }
+        if (j >= 1) {
+          ok = wait_bar(bar(C::B_VFULL + (j - 1) % C::STAGES), ((j - 1) / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          if (!ok) break;
+        }
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (j >= 1 && j <= n_t[t]) {
+            // PV_t(j-1): O_t += P_t V_{j-1}; P_t is read from TMEM (A operand)
+            ok = wait_bar(bar(C::B_PFULL + t), (j - 1) & 1, abort_flag, FAULT_MMA);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t v_stage = s_v + ((j - 1) % C::STAGES) * C::TILE_BYTES;
+            const uint32_t d_o = tmem + C::TMEM_O + t * D;
+            const uint32_t a_p = tmem + t * BN;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              // 16 keys = 16 rows of V = two 8-row swizzle groups (1024 B each)
+              const uint64_t bdesc = ptx::sdesc_sw128(v_stage + kk * 2048, C::CHUNK_BYTES, 1024);
+              ptx::mma_ts(d_o, a_p + kk * 8, bdesc, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(bar(C::B_ODONE + t));
+          }
+          if (j < n_t[t]) {
+            // S_t(j) = Q_t K_j^T
+            const uint32_t q_tile = s_q + t * C::TILE_BYTES;
+            const uint32_t k_stage = s_k + (j % C::STAGES) * C::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+              const uint64_t adesc = ptx::sdesc_sw128(q_tile + koff, 16, 1024);
+              const uint64_t bdesc = ptx::sdesc_sw128(k_stage + koff, 16, 1024);
+              ptx::mma_ss(tmem + t * BN, adesc, bdesc, C::IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(bar(C::B_SFULL + t));
+          }
+        }
+        if (!ok) break;
+        if (j < n_max) ptx::mma_commit(bar(C::B_KEMPTY + j % C::STAGES));
+        if (j >= 1) ptx::mma_commit(bar(C::B_VEMPTY + (j - 1) % C::STAGES));
+      }
+      if (!ok) {
+        // let every MMA already issued finish before TMEM is released
+        ptx::mma_commit(bar(C::B_DRAIN));
+        drain_wait(bar(C::B_DRAIN), 0);
+      }
+    }
+    __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
+    // ================================================================ softmax
+    const int t = warp >> 2;                  // Q tile of this warpgroup
+    const int r = (warp & 3) * 32 + lane;     // row within the tile = TMEM lane
+    const int i = row0 + t * BM + r;          // query row
+    const int n_tiles = t ? n_t1 : n_t0;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + t * BN;
+    const uint32_t t_o = tmem + lane_off + C::TMEM_O + t * D;
+    const float c = p.scale_log2;
+    float m_ref = -INFINITY;  // reference maximum, log2 units (scale folded in)
+    float l = 0.0f;           // running sum of 2^(c*s - m_ref)
+    bool ok = true;
+
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_SFULL + t), j & 1, abort_flag, FAULT_SOFTMAX));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) ptx::tmem_ld32(t_s + q4 * 32, sr[q4]);
+      ptx::tmem_wait_ld();
+
+      // mask: key-length boundary and the causal diagonal
+      const int j0 = j * BN;
+      const bool edge = (j0 + BN > kv_len) || (causal && j0 + BN - 1 > row0 + t * BM);
+      if (edge) {
+        int lim = kv_len - j0;
+        if (causal) lim = min(lim, i - j0 + 1);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            if (q4 * 32 + x >= lim) sr[q4][x] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int x = 0; x < 32; ++x) mx = fmaxf(mx, __uint_as_float(sr[q4][x]));
+      const float m_tile = mx * c;
+      const bool grow = m_tile > m_ref + kRescaleThreshold;
+      float alpha = 1.0f;
+      if (grow) {
+        alpha = ptx::ex2(m_ref - m_tile);  // 0 when m_ref is still -inf
+        l *= alpha;
+        m_ref = m_tile;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O_t must hold PV_t(j-1) before it is rescaled in place
+        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX));
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t o[32];
+          ptx::tmem_ld32(t_o + q4 * 32, o);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          ptx::tmem_st32(t_o + q4 * 32, o);
+        }
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[q4][x]), c, -m_use));
+          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[q4][x + 1]), c, -m_use));
+          part[q4] += p0 + p1;
+          pk[q4 >> 1][(q4 & 1) * 16 + (x >> 1)] = ptx::pack_bf16x2(p0, p1);
+        }
+      l += (part[0] + part[1]) + (part[2] + part[3]);
+      ptx::tmem_st32(t_s, pk[0]);
+      ptx::tmem_st32(t_s + 32, pk[1]);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_PFULL + t));
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    const bool row_valid = (row0 + t * BM < p.n_q) && (i < p.n_q);
+    if (ok && n_tiles > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (n_tiles - 1) & 1, abort_flag, FAULT_EPILOGUE));
+      if (ok) {
+        ptx::tc_fence_after();
+        const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+        uint16_t* orow = p.out + ((size_t)bh * p.n_q + (size_t)(row_valid ? i : 0)) * D;
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t o[32];
+          ptx::tmem_ld32(t_o + q4 * 32, o);
+          ptx::tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            w[x] = ptx::pack_bf16x2(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          }
+        }
+        if (row_valid && p.lse)
+          p.lse[(size_t)bh * p.n_q + i] = (l > 0.0f) ? (m_ref + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      }
+    } else if (ok && row_valid) {
+      // no legal key at all (key length 0): o = 0, lse = -inf
+      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.n_q + i) * D);
+#pragma unroll
+      for (int x = 0; x < D / 8; ++x) dst[x] = make_uint4(0, 0, 0, 0);
+      if (p.lse) p.lse[(size_t)bh * p.n_q + i] = -INFINITY;
+    }
+  }
+
+  // ---- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+CUresult encode_map(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int d, int n, int bh) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)n};
+  cuuint32_t box[3] = {64, (cuuint32_t)BM, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int D>
+int launch(const TcArgs& a, PFN_encodeTiled enc) {
+  using C = Cfg<D>;
+  // the shared-memory opt-in is per device; set it once for each device used
+  static std::atomic<bool> attr_done[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv;
+  if (encode_map(enc, &mq, a.q, D, a.n_q, a.B * a.H) != CUDA_SUCCESS ||
+      encode_map(enc, &mk, a.k, D, a.n_k, a.B * a.H) != CUDA_SUCCESS ||
+      encode_map(enc, &mv, a.v, D, a.n_k, a.B * a.H) != CUDA_SUCCESS)
+    return ATTN_ERR_UNSUPPORTED;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    attr_done[dev].store(true, std::memory_order_release);
+  }
+  Params p;
+  p.out = static_cast<uint16_t*>(a.out);
+  p.lse = a.lse;
+  p.key_lens = a.key_lens;
+  p.H = a.H;
+  p.n_q = a.n_q;
+  p.n_k = a.n_k;
+  p.mask_mode = a.mask_mode;
+  p.BH = a.B * a.H;
+  p.num_qblocks = (a.n_q + 2 * BM - 1) / (2 * BM);
+  p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
+  const long long grid = (long long)p.BH * p.num_qblocks;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  attn_fwd_tc_kernel<D><<<(unsigned)grid, THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
+  return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc) {
+  if (a.d == 64) return launch<64>(a, enc);
+  if (a.d == 128) return launch<128>(a, enc);
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+int read_fault_word(cudaStream_t stream, int clear, uint32_t* out) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_fault_word, sizeof w) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (clear) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (out) *out = w;
+  return w ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+}  // namespace attn

@@ -1,0 +1,50 @@
+// attn_internal.h -- declarations shared by the host API and the kernels of
+// libattn_gb300.so (not part of the public C ABI; see include/attn_gb300.h).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "attn_gb300.h"
+
+namespace attn {
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (no -lcuda link).
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Validated arguments of one bf16 call.
+struct TcArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int B, H, n_q, n_k, d;
+  float scale;
+  int mask_mode;
+  const int32_t* key_lens;
+  cudaStream_t stream;
+};
+
+// Validated arguments of one fp32 call.
+struct F32Args {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  float* lse;
+  int B, H, n_q, n_k, d_k, d_v;
+  float scale;
+  int mask_mode;
+  const int32_t* key_lens;
+  cudaStream_t stream;
+};
+
+int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc);   // attn_fwd_tc.cu
+int launch_attn_f32(const F32Args& a);                       // attn_fwd_f32.cu
+int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd_tc.cu
+
+}  // namespace attn
