@@ -1,0 +1,392 @@
+"""Attention forward benchmark: TFLOP/s on one GB300 and the fraction of the dense
+bf16 tensor-core peak.
+
+Default workload: long-sequence causal self-attention, B=2, h=16, n=8192,
+d_k=d_v=64, bf16 inputs N(0,1) x 0.5 (the pages' O(n^2 d) scaling case). One step
+is one attn_fwd call over the whole batch (all steps of the hot path: Q/K/V
+tiles in, QK^T, scale, mask, online softmax, PV, normalisation and the bf16 /
+lse stores). FLOPs are algorithmic: 2 (d_k + d_v) per legal query-key pair.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (independent shards of B*h, no collective on the data path; weak scaling),
+the timed region is bracketed by a barrier and a synchronize on both sides, and
+the time is the maximum over ranks. Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on bounded row samples of the same
+workload (rank 0 only; other ranks exit without work).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from transformer_scaled_dot_mha_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "long_causal_b2_h16_n8192_d64"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the tensor-core kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
+# kernel sources it was measured on; reported only while the sources match.
+NCU_TRAFFIC = {
+    # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
+    ("long_causal_b2_h16_n8192_d64", "d94749fd0342898a"): 143211776,
+}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_fwd_tc.cu", "ptx_sm103.cuh"):
+        with open(os.path.join(ROOT, "transformer_scaled_dot_mha_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def mask_name(mode):
+    return {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[mode]
+
+
+def config_of(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "h": w.H, "n_q": w.n_q, "n_k": w.n_k, "d_k": w.d_k, "d_v": w.d_v,
+           "mask": mask_name(w.mask_mode), "inputs": f"N(0,1) x {w.input_scale}, seed {w.seed}",
+           "flops": "algorithmic: 2*(d_k+d_v) per legal (query, key) pair"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for ln in out.splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) == 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples arrive every 100 ms; keep the loaded ones (the timed region is short)
+        loaded = [r for r in rows if float(r[3]) > 200.0] or rows
+        sm = [float(r[1]) for r in loaded]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(float(r[2]) for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded), "power_w_max": max(float(r[3]) for r in loaded)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def sample_row_ids(w, rng_seed=7):
+    """Row ids spread over all heads and positions of the workload."""
+    rng = np.random.Generator(np.random.PCG64(rng_seed))
+    return rng.permutation(w.B * w.H * w.n_q).astype(np.int64)
+
+
+def oracle_rows_flops(w, ids, key_lens):
+    i = ids % w.n_q
+    b = ids // (w.H * w.n_q)
+    lim = np.full(ids.shape, w.n_k, np.int64)
+    if w.mask_mode & W.MASK_KEY_PADDING:
+        lim = np.minimum(lim, key_lens[b])
+    if w.mask_mode & W.MASK_CAUSAL:
+        lim = np.minimum(lim, i + 1)
+    return float(2 * (w.d_k + w.d_v) * lim.sum())
+
+
+def time_oracle(w, inputs, ids, threads):
+    import oracle
+
+    if not os.path.exists(oracle.LIB):
+        oracle.build()
+    orc = oracle.Oracle()
+    q, k, v, kl = inputs
+    t0 = time.perf_counter()
+    orc.attention_rows(q, k, v, w.scale, ids, w.mask_mode, kl, n_threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, inputs, target_s=12.0):
+    """The oracle as it stands, on a bounded sample of rows of the same workload."""
+    threads = os.cpu_count() or 1
+    ids_all = sample_row_ids(w)
+    n = max(threads, 16)
+    dt = time_oracle(w, inputs, ids_all[:n], threads)
+    while dt < 0.5 and n < ids_all.size:
+        n = min(ids_all.size, n * 4)
+        dt = time_oracle(w, inputs, ids_all[:n], threads)
+    n = int(min(ids_all.size, max(n, n * target_s / max(dt, 1e-9))))
+    ids = ids_all[:n]
+    dt = time_oracle(w, inputs, ids, threads)
+    flops = oracle_rows_flops(w, ids, inputs[3])
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} query rows drawn uniformly from all {w.B * w.H * w.n_q} rows of the workload "
+                      f"({flops / 1e9:.2f} GFLOP algorithmic), fp64 C oracle, {dt:.2f} s wall"}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from transformer_scaled_dot_mha_gb300 import attn
+
+    attn.lib()
+    q, k, v, kl = W.make_inputs(w)
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    kld = torch.from_numpy(kl).to(dev)
+    out = torch.empty((w.B, w.H, w.n_q, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.n_q), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    key_lens = kld if w.mask_mode & W.MASK_KEY_PADDING else None
+
+    def step():
+        attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} during warm-up")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for e0, e1 in evs:
+        flush.zero_()  # L2 flush between timed steps, outside the events
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop() if rank == 0 else None
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = float(sum(times_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} in the timed region")
+
+    flops_step = w.algorithmic_flops(kl)
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+
+    # ---- end to end through the public call: pinned host buffers in, result out
+    e2e = run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world)
+
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    achieved = flops_step / (ms_per_step / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get((w.name, src_hash))
+    line = {
+        "metric": "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, {"l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB memset)",
+                                "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
+                                "dense_equivalent_tflops": round(world * w.dense_flops() * args.steps /
+                                                                 (total_ms / 1e3) / 1e12, 2)}),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"bf16_tflops (burst) of {peak_src}", "kernel": "attn_fwd_tc_kernel",
+                     "kernel_source": src_hash},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, (q, k, v, kl))
+    return line
+
+
+def run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world):
+    """Same metric through attn_fwd with host buffers: pinned H2D of Q/K/V (and
+    key lengths), the kernel, and D2H of the output, all inside the events."""
+    import torch
+
+    pin = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    qh, kh, vh = pin(q), pin(k), pin(v)
+    klh = torch.from_numpy(kl).pin_memory()
+    outh = torch.empty((w.B, w.H, w.n_q, w.d_v), dtype=torch.bfloat16).pin_memory()
+    qd, kd, vd = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
+    kld = torch.empty_like(klh, device=dev)
+    out = torch.empty_like(outh, device=dev)
+    use_kl = bool(w.mask_mode & W.MASK_KEY_PADDING)
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        if use_kl:
+            kld.copy_(klh, non_blocking=True)
+        attn.attn_fwd(qd, kd, vd, out, None, w.scale, w.mask_mode, kld if use_kl else None, stream)
+        outh.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (klh.numel() * 4 if use_kl else 0)
+    d2h = outh.numel() * outh.element_size()
+    return {"value": round(world * flops_step / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
+            "steps": steps, "how": "pinned host buffers, copies and kernel on one stream, CUDA events"}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    threads = os.cpu_count() or 1
+    inputs = W.make_inputs(w)
+    ids_all = sample_row_ids(w)
+    # per-step sample sized so warm-up + steps take about a minute in total
+    budget_s = 60.0 / max(1, args.steps + args.warmup)
+    n = threads
+    dt = time_oracle(w, inputs, ids_all[:n], threads)
+    n = int(max(1, min(ids_all.size // max(1, args.steps + args.warmup), n * budget_s / max(dt, 1e-9))))
+    pos = 0
+    for _ in range(args.warmup):
+        time_oracle(w, inputs, ids_all[pos:pos + n], threads)
+        pos = (pos + n) % max(1, ids_all.size - n)
+    total_s, total_flops = 0.0, 0.0
+    for _ in range(args.steps):
+        ids = ids_all[pos:pos + n]
+        total_s += time_oracle(w, inputs, ids, threads)
+        total_flops += oracle_rows_flops(w, ids, inputs[3])
+        pos = (pos + n) % max(1, ids_all.size - n)
+    value = total_flops / total_s / 1e12
+    sample = (f"each step: {n} query rows drawn uniformly from all {w.B * w.H * w.n_q} rows of the workload, "
+              f"fp64 C oracle on {threads} host threads")
+    return {"impl": "reference", "metric": "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = W.WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        ap.error("the benchmark times the bf16 tensor-core path; pick a bf16 workload")
+    world, rank, _ = dist_env()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 must be launched with torchrun (one process per GPU)")
+    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
