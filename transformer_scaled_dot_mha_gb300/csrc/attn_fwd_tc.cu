@@ -12,21 +12,25 @@
 //
 // Work decomposition. One CTA owns 256 query rows of one (b, h): two 128-row Q
 // tiles. It streams 128-key K/V tiles through a shared-memory ring filled by TMA.
-// Warp roles (384 threads = three warpgroups):
-//   warps 0-3  softmax warpgroup for Q tile 0 (thread = query row = TMEM lane)
-//   warps 4-7  softmax warpgroup for Q tile 1
-//   warp  8    TMA producer (one lane)
-//   warp  9    MMA issuer (one lane); also allocates / frees TMEM
-//   warps 10-11 idle members of the control warpgroup
-// The control warpgroup hands registers to the softmax warpgroups (setmaxnreg:
-// 56 and 224 per thread; 128*56 + 256*224 = 384*168, the launch allocation).
-// Tensor memory (512 columns x 128 lanes of 32 bit):
-//   [0,128)   S0 = Q0 K_j^T (fp32); P0 (bf16 pairs) overwrites its first 64 columns
-//   [128,256) S1 / P1
-//   [256, 256+D) O0 accumulator, [256+D, 256+2D) O1 accumulator (fp32)
-// Per K/V tile j the MMA issuer runs, in order,
-//   PV0(j-1): O0 += P0 V_{j-1};  S0(j) = Q0 K_j^T;  PV1(j-1);  S1(j)
-// so each softmax warpgroup works while the tensor core serves the other tile.
+// Warps 0-3 and 4-7 are the softmax warpgroups of Q tiles 0 and 1 (thread =
+// query row = TMEM lane); warp 8 is the TMA producer; warp 9 allocates and frees
+// TMEM. The control warps hand registers to the softmax warps with setmaxnreg.
+//
+// Tensor memory (512 columns x 128 lanes of 32 bit), fp32 S and O, bf16-pair P:
+//   D = 64:  S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0 [384,448) O1 [448,512)
+//   D = 128: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_t overwrites the
+//            first 64 columns of S_t.
+//
+// D = 64 (512 threads): P has its own columns, so a softmax warpgroup releases
+// S_t as soon as it has loaded it. Four issuer warps -- 9 + t issues S_t, 11 + t
+// issues PV_t -- run S_t(j+1) = Q_t K_{j+1}^T while the softmax of tile j is still
+// exponentiating, and PV_t(j) during the softmax of tile j+1; the softmax waits
+// for PV_t(j-1) only before it overwrites P_t. K/V stages are released by two
+// arrivals (both Q tiles).
+// D = 128 (384 threads): P lives in S, so S_t(j) must follow PV_t(j-1). One issuer
+// (warp 9) runs, in order, PV0(j-1), S0(j), PV1(j-1), S1(j): each softmax
+// warpgroup works while the tensor core serves the other tile.
+//
 // The softmax rescales O only when a row maximum grows by more than 2^8 (a lazy
 // reference maximum); the final O / l is exact whatever reference was used.
 //
@@ -52,11 +56,8 @@ namespace {
 
 constexpr int BM = 128;  // query rows per Q tile (= TMEM lanes)
 constexpr int BN = 128;  // keys per K/V tile
-constexpr int THREADS = 384;
-constexpr int REGS_CONTROL = 56;
-constexpr int REGS_SOFTMAX = 224;
 constexpr int WARP_LOAD = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA0 = 9;  // MMA issuer of Q tile 0; WARP_MMA0 + 1 issues for Q tile 1
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain copies in flight
@@ -80,17 +81,29 @@ struct Cfg {
   static constexpr int B_KEMPTY = B_KFULL + STAGES;
   static constexpr int B_VFULL = B_KEMPTY + STAGES;
   static constexpr int B_VEMPTY = B_VFULL + STAGES;
-  static constexpr int B_SFULL = B_VEMPTY + STAGES;  // [2]
-  static constexpr int B_PFULL = B_SFULL + 2;        // [2]
-  static constexpr int B_ODONE = B_PFULL + 2;        // [2]
-  static constexpr int B_DRAIN = B_ODONE + 2;
-  static constexpr int NUM_BARS = B_DRAIN + 1;
+  static constexpr int B_SFULL = B_VEMPTY + STAGES;  // [2] S_t computed
+  static constexpr int B_SFREE = B_SFULL + 2;        // [2] S_t loaded by the softmax (SEP_P only)
+  static constexpr int B_PFULL = B_SFREE + 2;        // [2] P_t stored
+  static constexpr int B_ODONE = B_PFULL + 2;        // [2] PV_t completed
+  static constexpr int B_DRAIN = B_ODONE + 2;        // [4] MMA drain after an abort, one per issuer
+  static constexpr int NUM_BARS = B_DRAIN + 4;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TMEM_O = 2 * BN;
+  static constexpr bool SEP_P = (D == 64);  // P has its own TMEM columns
+  // SEP_P: four MMA issuers (S and PV per Q tile) -> 16 warps; else one issuer, 12 warps.
+  // Register split (setmaxnreg): control warps give registers to the softmax warps;
+  // the total stays equal to the launch allocation.
+  static constexpr int THREADS = SEP_P ? 512 : 384;
+  static constexpr int REGS_CONTROL = SEP_P ? 40 : 56;
+  static constexpr int REGS_SOFTMAX = SEP_P ? 216 : 224;
+  static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;  // 128 or 168 per thread
+  static_assert((THREADS - 256) * REGS_CONTROL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
+  static constexpr uint32_t TMEM_P = SEP_P ? 2 * BN : 0;          // + t * (SEP_P ? 64 : BN)
+  static constexpr uint32_t TMEM_P_STRIDE = SEP_P ? BN / 2 : BN;
+  static constexpr uint32_t TMEM_O = SEP_P ? 3 * BN : 2 * BN;     // + t * D
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);  // Q, K both K-major
   static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);   // V is MN-major
   static_assert(TMEM_O + 2 * D <= TMEM_COLS, "TMEM budget");
@@ -138,7 +151,7 @@ __device__ __forceinline__ int tiles_for(int r0, int n_q, int kv_tiles, bool cau
 }
 
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D>;
@@ -171,20 +184,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(bar(C::B_KFULL + s), 1);
-      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);
+      ptx::mbar_init(bar(C::B_KEMPTY + s), C::SEP_P ? 2 : 1);  // one arrival per MMA issuer
       ptx::mbar_init(bar(C::B_VFULL + s), 1);
-      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), C::SEP_P ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(C::B_SFULL + t), 1);
-      ptx::mbar_init(bar(C::B_PFULL + t), BM);  // every softmax thread arrives
+      ptx::mbar_init(bar(C::B_SFREE + t), BM);  // every softmax thread arrives
+      ptx::mbar_init(bar(C::B_PFULL + t), BM);
       ptx::mbar_init(bar(C::B_ODONE + t), 1);
     }
-    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    for (int x = 0; x < 4; ++x) ptx::mbar_init(bar(C::B_DRAIN + x), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == WARP_MMA) {
+  if (warp == WARP_MMA0) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CONTROL));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CONTROL));
     if (warp == WARP_LOAD) {
     // ================================================================ producer
     if (lane == 0 && n_max > 0) {
@@ -244,10 +258,73 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     __syncwarp();
-    } else if (warp == WARP_MMA) {
-    // ================================================================ MMA issuer
-    if (lane == 0 && n_max > 0) {
-      const int n_t[2] = {n_t0, n_t1};
+    } else if (warp >= WARP_MMA0 && warp < WARP_MMA0 + 4) {
+    // ================================================================ MMA issuers
+    // SEP_P: warp 9 + t issues S_t, warp 11 + t issues PV_t. Otherwise warp 9 issues all.
+    const int role = warp - WARP_MMA0;
+    const int t = role & 1;  // Q tile
+    const int n_t = t ? n_t1 : n_t0;
+    const int n_o = t ? n_t0 : n_t1;  // tiles of the other Q tile
+    // a K/V stage the other Q tile never reads is released twice by this issuer
+    auto release = [&](int b0, int j) {
+      ptx::mma_commit(bar(b0 + j % C::STAGES));
+      if (j >= n_o) ptx::mma_commit(bar(b0 + j % C::STAGES));
+    };
+    if (C::SEP_P && role < 2 && lane == 0 && n_t > 0) {
+      // S_t(j) = Q_t K_j^T, as soon as K_j has landed and the softmax has loaded S_t(j-1)
+      const uint32_t q_tile = s_q + t * C::TILE_BYTES;
+      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
+      for (int j = 0; j < n_t && ok; ++j) {
+        ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA) &&
+             (j == 0 || wait_bar(bar(C::B_SFREE + t), (j - 1) & 1, abort_flag, FAULT_MMA));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t k_stage = s_k + (j % C::STAGES) * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          ptx::mma_ss(tmem + t * BN, ptx::sdesc_sw128(q_tile + koff, 16, 1024),
+                      ptx::sdesc_sw128(k_stage + koff, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_SFULL + t));
+        release(C::B_KEMPTY, j);
+      }
+      if (!ok) {
+        // let every MMA already issued finish before TMEM is released
+        ptx::mma_commit(bar(C::B_DRAIN + role));
+        drain_wait(bar(C::B_DRAIN + role), 0);
+      }
+    }
+    if (C::SEP_P && role >= 2 && lane == 0 && n_t > 0) {
+      // O_t += P_t V_j once the softmax has stored P_t(j); P_t is the A operand, read from TMEM
+      const uint32_t a_p = tmem + C::TMEM_P + t * C::TMEM_P_STRIDE;
+      const uint32_t d_o = tmem + C::TMEM_O + t * D;
+      bool ok = true;
+      for (int j = 0; j < n_t && ok; ++j) {
+        ok = wait_bar(bar(C::B_PFULL + t), j & 1, abort_flag, FAULT_MMA) &&
+             wait_bar(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t v_stage = s_v + (j % C::STAGES) * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys = 16 rows of V = two 8-row swizzle groups
+          ptx::mma_ts(d_o, a_p + kk * 8, ptx::sdesc_sw128(v_stage + kk * 2048, C::CHUNK_BYTES, 1024), C::IDESC_PV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(bar(C::B_ODONE + t));
+        release(C::B_VEMPTY, j);
+      }
+      if (!ok) {
+        ptx::mma_commit(bar(C::B_DRAIN + role));
+        drain_wait(bar(C::B_DRAIN + role), 0);
+      }
+    }
+    if (!C::SEP_P && role == 0 && lane == 0 && n_max > 0) {
+      // P_t lives in S_t, so S_t(j) must follow PV_t(j-1). One issuer runs, in order,
+      //   PV0(j-1), S0(j), PV1(j-1), S1(j)
+      // keeping each tile's hand-off short while the other tile's softmax runs.
+      // (This issuer is on the critical path: keep its loop lean; the 2-way tile loop
+      // must stay a plain counted loop so that it unrolls.)
+      const int n_tt[2] = {n_t0, n_t1};
       bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
       ptx::tc_fence_after();
       for (int j = 0; j <= n_max && ok; ++j) {
@@ -260,35 +337,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!ok) break;
         }
         ptx::tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (j >= 1 && j <= n_t[t]) {
-            // PV_t(j-1): O_t += P_t V_{j-1}; P_t is read from TMEM (A operand)
-            ok = wait_bar(bar(C::B_PFULL + t), (j - 1) & 1, abort_flag, FAULT_MMA);
+        for (int tt = 0; tt < 2; ++tt) {
+          if (j >= 1 && j <= n_tt[tt]) {
+            ok = wait_bar(bar(C::B_PFULL + tt), (j - 1) & 1, abort_flag, FAULT_MMA);
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t v_stage = s_v + ((j - 1) % C::STAGES) * C::TILE_BYTES;
-            const uint32_t d_o = tmem + C::TMEM_O + t * D;
-            const uint32_t a_p = tmem + t * BN;
+            const uint32_t d_o = tmem + C::TMEM_O + tt * D;
+            const uint32_t a_p = tmem + tt * BN;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
-              // 16 keys = 16 rows of V = two 8-row swizzle groups (1024 B each)
               const uint64_t bdesc = ptx::sdesc_sw128(v_stage + kk * 2048, C::CHUNK_BYTES, 1024);
               ptx::mma_ts(d_o, a_p + kk * 8, bdesc, C::IDESC_PV, (j > 1 || kk > 0) ? 1u : 0u);
             }
-            ptx::mma_commit(bar(C::B_ODONE + t));
+            ptx::mma_commit(bar(C::B_ODONE + tt));
           }
-          if (j < n_t[t]) {
-            // S_t(j) = Q_t K_j^T
-            const uint32_t q_tile = s_q + t * C::TILE_BYTES;
+          if (j < n_tt[tt]) {
+            const uint32_t q_tile = s_q + tt * C::TILE_BYTES;
             const uint32_t k_stage = s_k + (j % C::STAGES) * C::TILE_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
               const uint64_t adesc = ptx::sdesc_sw128(q_tile + koff, 16, 1024);
               const uint64_t bdesc = ptx::sdesc_sw128(k_stage + koff, 16, 1024);
-              ptx::mma_ss(tmem + t * BN, adesc, bdesc, C::IDESC_S, kk > 0 ? 1u : 0u);
+              ptx::mma_ss(tmem + tt * BN, adesc, bdesc, C::IDESC_S, kk > 0 ? 1u : 0u);
             }
-            ptx::mma_commit(bar(C::B_SFULL + t));
+            ptx::mma_commit(bar(C::B_SFULL + tt));
           }
         }
         if (!ok) break;
@@ -296,7 +370,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (j >= 1) ptx::mma_commit(bar(C::B_VEMPTY + (j - 1) % C::STAGES));
       }
       if (!ok) {
-        // let every MMA already issued finish before TMEM is released
         ptx::mma_commit(bar(C::B_DRAIN));
         drain_wait(bar(C::B_DRAIN), 0);
       }
@@ -304,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_SOFTMAX));
     // ================================================================ softmax
     const int t = warp >> 2;                  // Q tile of this warpgroup
     const int r = (warp & 3) * 32 + lane;     // row within the tile = TMEM lane
@@ -312,6 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_tiles = t ? n_t1 : n_t0;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_off + t * BN;
+    const uint32_t t_p = tmem + lane_off + C::TMEM_P + t * C::TMEM_P_STRIDE;
     const uint32_t t_o = tmem + lane_off + C::TMEM_O + t * D;
     const float c = p.scale_log2;
     float m_ref = -INFINITY;  // reference maximum, log2 units (scale folded in)
@@ -326,6 +400,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) ptx::tmem_ld32(t_s + q4 * 32, sr[q4]);
       ptx::tmem_wait_ld();
+      if (C::SEP_P) {  // S_t may now be overwritten by S_t(j+1)
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_SFREE + t));
+      }
 
       // mask: key-length boundary and the causal diagonal
       const int j0 = j * BN;
@@ -339,11 +417,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int x = 0; x < 32; ++x)
             if (q4 * 32 + x >= lim) sr[q4][x] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // row maximum: eight independent 3-input max chains over 16 columns each
+      auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
+      float mc[8];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+      for (int a = 0; a < 8; ++a) {
+        mc[a] = fmaxf(col(a, 0), col(a, 1));
 #pragma unroll
-        for (int x = 0; x < 32; ++x) mx = fmaxf(mx, __uint_as_float(sr[q4][x]));
+        for (int x = 2; x < 16; x += 2) mc[a] = ptx::max3(mc[a], col(a, x), col(a, x + 1));
+      }
+      const float mx = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
       const float m_tile = mx * c;
       const bool grow = m_tile > m_ref + kRescaleThreshold;
       float alpha = 1.0f;
@@ -352,10 +435,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         l *= alpha;
         m_ref = m_tile;
       }
+      bool pv_done = (j == 0);  // PV_t(j-1) known to have completed
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O_t must hold PV_t(j-1) before it is rescaled in place
         ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX));
         if (!ok) break;
+        pv_done = true;
         ptx::tc_fence_after();
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -368,20 +453,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(s*c - m) for pairs of columns: one packed FMA, two MUFU exp2, one
+      // packed add into one of four running pair-sums, one bf16x2 conversion
+      const uint64_t c2 = ptx::f2_pack(c, c);
+      const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+      uint64_t part[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
-          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[q4][x]), c, -m_use));
-          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[q4][x + 1]), c, -m_use));
-          part[q4] += p0 + p1;
+          const uint64_t sx = ptx::f2_pack(__uint_as_float(sr[q4][x]), __uint_as_float(sr[q4][x + 1]));
+          float a0, a1;
+          ptx::f2_unpack(ptx::f2_fma(sx, c2, negm2), a0, a1);
+          const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+          part[q4] = ptx::f2_add(part[q4], ptx::f2_pack(p0, p1));
           pk[q4 >> 1][(q4 & 1) * 16 + (x >> 1)] = ptx::pack_bf16x2(p0, p1);
         }
-      l += (part[0] + part[1]) + (part[2] + part[3]);
-      ptx::tmem_st32(t_s, pk[0]);
-      ptx::tmem_st32(t_s + 32, pk[1]);
+      float l0, l1;
+      ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
+      l += l0 + l1;
+      if (C::SEP_P && !pv_done) {
+        // P_t is still the A operand of PV_t(j-1) until that MMA completes
+        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX));
+        if (!ok) break;
+        ptx::tc_fence_after();
+      }
+      ptx::tmem_st32(t_p, pk[0]);
+      ptx::tmem_st32(t_p + 32, pk[1]);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_PFULL + t));
@@ -425,7 +524,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- teardown
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == WARP_MMA) {
+  if (warp == WARP_MMA0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -472,7 +571,7 @@ int launch(const TcArgs& a, PFN_encodeTiled enc) {
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   const long long grid = (long long)p.BH * p.num_qblocks;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_fwd_tc_kernel<D><<<(unsigned)grid, THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -46,6 +46,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Arrive once `dep` has been computed: the operand ties the arrival to the
+// instructions that produce it, so they cannot be scheduled after it.
+__device__ __forceinline__ void mbar_arrive_after(uint32_t bar, float dep) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t// %1" ::"r"(bar), "f"(dep) : "memory");
+}
+
+// Returns x unchanged, through a volatile instruction: everything computed from
+// the result stays after this point in program order.
+__device__ __forceinline__ float pin(float x) {
+  asm volatile("mov.b32 %0, %0;" : "+f"(x));
+  return x;
+}
+
 // One non-blocking-ish probe: true once the phase with parity `parity` has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -175,6 +188,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of floats in one 64-bit register (x in the low half).
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& x, float& y) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+// Element-wise a*b + c and a + b on float pairs (one instruction each).
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // ---------------------------------------------------------------- descriptors
