@@ -72,6 +72,28 @@ def dist_env():
     return world, rank, local
 
 
+def shard_seed(w, rank: int) -> int:
+    """Each rank draws its own shard of (b, h) problems; rank 0 keeps the workload's seed."""
+    return w.seed + 1000 * rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a per-rank scalar over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tflops(flops_per_rank_step: float, steps: int, max_total_ms: float, world: int) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (max_total_ms / 1e3) / 1e12
+
+
 def mask_name(mode):
     return {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[mode]
 
@@ -96,7 +118,6 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -106,9 +127,6 @@ class ClockSampler:
         except (FileNotFoundError, OSError):
             self.proc = None
         time.sleep(0.3)
-
-    def mark(self, which):
-        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -198,7 +216,7 @@ def run_ours(args, w):
     from transformer_scaled_dot_mha_gb300 import attn
 
     attn.lib()
-    q, k, v, kl = W.make_inputs(w)
+    q, k, v, kl = W.make_inputs(w, shard_seed(w, rank))
     to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     kld = torch.from_numpy(kl).to(dev)
@@ -238,18 +256,14 @@ def run_ours(args, w):
     wall = time.perf_counter() - t_wall0
     clk = clocks.stop() if rank == 0 else None
     times_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = float(sum(times_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times_ms), dev)
     st, code = attn.attn_fault_status(stream)
     if st != attn.ATTN_OK:
         raise RuntimeError(f"kernel fault record {code:#x} in the timed region")
 
     flops_step = w.algorithmic_flops(kl)
     ms_per_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    value = weak_scaling_tflops(flops_step, args.steps, total_ms, world)
 
     # ---- end to end through the public call: pinned host buffers in, result out
     e2e = run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world)
@@ -319,14 +333,10 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dev)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (klh.numel() * 4 if use_kl else 0)
     d2h = outh.numel() * outh.element_size()
-    return {"value": round(world * flops_step / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(weak_scaling_tflops(flops_step, 1, ms, world), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
             "steps": steps, "how": "pinned host buffers, copies and kernel on one stream, CUDA events"}
 
