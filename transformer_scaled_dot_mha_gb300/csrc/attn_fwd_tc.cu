@@ -400,10 +400,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) ptx::tmem_ld32(t_s + q4 * 32, sr[q4]);
       ptx::tmem_wait_ld();
-      if (C::SEP_P) {  // S_t may now be overwritten by S_t(j+1)
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(C::B_SFREE + t));
-      }
 
       // mask: key-length boundary and the causal diagonal
       const int j0 = j * BN;
@@ -428,6 +424,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       const float mx = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
       const float m_tile = mx * c;
+      if (C::SEP_P) {  // S_t may now be overwritten by S_t(j+1)
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_SFREE + t));
+      }
       const bool grow = m_tile > m_ref + kRescaleThreshold;
       float alpha = 1.0f;
       if (grow) {
