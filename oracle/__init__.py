@@ -29,7 +29,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "attn_oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
-MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_DECODE = 0, 1, 2, 4
 _DTYPES = {np.dtype(np.float64): 0, np.dtype(np.float32): 1, np.dtype(np.uint16): 2}
 _CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
 
@@ -75,7 +75,7 @@ class Oracle:
 
     @staticmethod
     def _lens(mask_mode, key_lens, B):
-        if not (mask_mode & MASK_KEY_PADDING):
+        if not (mask_mode & (MASK_KEY_PADDING | MASK_DECODE)):
             return None
         kl = np.ascontiguousarray(key_lens, dtype=np.int32)
         if kl.shape != (B,):
@@ -141,6 +141,9 @@ def legal_mask(B, n_q, n_k, mask_mode, key_lens=None) -> np.ndarray:
         ok &= (j <= i)[None, None]
     if mask_mode & MASK_KEY_PADDING:
         ok &= (j[None, None] < np.asarray(key_lens).reshape(B, 1, 1, 1))
+    if mask_mode & MASK_DECODE:  # query i sits at position key_len - n_q + i
+        pos = np.asarray(key_lens).reshape(B, 1, 1, 1) - n_q + i[None, None]
+        ok &= (j[None, None] <= pos)
     return ok
 
 

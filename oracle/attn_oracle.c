@@ -14,7 +14,8 @@
  *     lse = m + ln l
  * Sources: "Attention Is All You Need" (rockcohen.cc) section 3.2 (softmax,
  * shift invariance), section 5.1 (Eq. 1 and the 1/sqrt(d_k) scale), sections
- * 5.3 and 6.3 (-inf at the softmax input, exact-zero weights); vlmlib.cn paper
+ * 5.3 and 6.3 (-inf at the softmax input, exact-zero weights; the causal mask that
+ * makes step-by-step generation legal, used here for the decode mask); vlmlib.cn paper
  * summary, "scaled dot-product attention" and "multi-head attention" (heads are
  * independent attention calls); attention-paper-guide section 03.2 (the
  * four steps: dot products, scale, softmax, weighted sum of V).
@@ -58,6 +59,7 @@ static double elem(const void* base, int dtype, long long idx) {
 static int legal(const problem* p, int b, int i, int j) {
   if ((p->mask_mode & ORACLE_MASK_CAUSAL) && j > i) return 0;
   if ((p->mask_mode & ORACLE_MASK_KEY_PADDING) && j >= p->key_lens[b]) return 0;
+  if ((p->mask_mode & ORACLE_MASK_DECODE) && j > p->key_lens[b] - p->n_q + i) return 0;
   return 1;
 }
 
@@ -142,8 +144,9 @@ static int check(const problem* p) {
   if (!p->q || !p->k) return -1;
   if (p->dtype < ORACLE_F64 || p->dtype > ORACLE_BF16) return -1;
   if (p->B <= 0 || p->H <= 0 || p->n_q <= 0 || p->n_k <= 0 || p->d_k <= 0 || p->d_v < 0) return -1;
-  if ((p->mask_mode & ~(ORACLE_MASK_CAUSAL | ORACLE_MASK_KEY_PADDING)) != 0) return -1;
-  if ((p->mask_mode & ORACLE_MASK_KEY_PADDING) && !p->key_lens) return -1;
+  if ((p->mask_mode & ~(ORACLE_MASK_CAUSAL | ORACLE_MASK_KEY_PADDING | ORACLE_MASK_DECODE)) != 0) return -1;
+  if ((p->mask_mode & ORACLE_MASK_CAUSAL) && (p->mask_mode & ORACLE_MASK_DECODE)) return -1;
+  if ((p->mask_mode & (ORACLE_MASK_KEY_PADDING | ORACLE_MASK_DECODE)) && !p->key_lens) return -1;
   return 0;
 }
 

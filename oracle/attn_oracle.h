@@ -14,7 +14,13 @@
  *   exact 0 -- rockcohen.cc sections 5.3 and 6.3.
  *   Causal (decoder self-attention): key j is illegal for query i when j > i.
  *   Key padding (encoder, cross-attention): key j is illegal when j >= key_lens[b]
- *   (right padding; the reading of the csdn blog's padding mask, see DESIGN).
+ *   (right padding; the reading of the csdn blog's padding mask).
+ *   Decode (autoregressive generation, one step of n_q new queries against a key
+ *   cache of key_lens[b] entries): query i sits at position key_lens[b] - n_q + i
+ *   and key j is illegal when j > key_lens[b] - n_q + i. This is the causal mask
+ *   of decoder self-attention applied to the newest n_q positions (attention-paper-
+ *   guide section 05 and rockcohen.cc section 6.3: generation proceeds one position
+ *   at a time and each position sees only positions up to itself).
  *
  * Conventions chosen where the pages are silent:
  *   - a row with no legal key returns o = 0 and lse = -inf;
@@ -34,10 +40,11 @@ extern "C" {
 /* element type of the Q/K/V input arrays */
 enum { ORACLE_F64 = 0, ORACLE_F32 = 1, ORACLE_BF16 = 2 /* raw bf16 bit patterns, uint16 */ };
 /* mask bits */
-enum { ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_KEY_PADDING = 2 };
+enum { ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_KEY_PADDING = 2, ORACLE_MASK_DECODE = 4 };
 
 /* Full output. out: B*H*n_q*d_v doubles; lse: B*H*n_q doubles or NULL.
- * key_lens: B ints, required iff mask bit 2 is set. n_threads <= 0 means 1.
+ * key_lens: B ints, required iff mask bit 2 or 4 is set. Bits 1 and 4 are exclusive.
+ * n_threads <= 0 means 1.
  * Returns 0, or -1 on an invalid argument. */
 int oracle_attn(const void* q, const void* k, const void* v, int dtype,
                 int B, int H, int n_q, int n_k, int d_k, int d_v, double scale,

@@ -20,7 +20,7 @@ import numpy as np
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-C, P = oracle.MASK_CAUSAL, oracle.MASK_KEY_PADDING
+C, P, DEC = oracle.MASK_CAUSAL, oracle.MASK_KEY_PADDING, oracle.MASK_DECODE
 
 
 def _golden(name):
@@ -273,6 +273,57 @@ def pin_input_widening(orc):
         assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
     # bf16 1.0 is 0x3F80, -2.0 is 0xC000
     assert np.array_equal(oracle.widen(np.array([0x3F80, 0xC000], np.uint16)), [1.0, -2.0])
+
+
+# ---------------------------------------------------------------- decode (one generation step)
+def pin_decode_is_causal_suffix(orc):
+    """A decode step of n_q new queries against len keys is exactly the last n_q rows
+    of causal self-attention over the first len positions (rockcohen.cc section 6.3:
+    each position sees the prefix up to itself; generation adds positions one at a
+    time)."""
+    rng = np.random.Generator(np.random.PCG64(30))
+    B, H, n_q, n_max, dk, dv = 3, 2, 4, 11, 3, 5
+    q = rng.standard_normal((B, H, n_q, dk))
+    k = rng.standard_normal((B, H, n_max, dk))
+    v = rng.standard_normal((B, H, n_max, dv))
+    lens = np.array([11, 7, 4], np.int32)
+    out, lse = orc.attention(q, k, v, 0.45, DEC, lens)
+    for b, L in enumerate(lens):
+        qf = np.concatenate([rng.standard_normal((1, H, L - n_q, dk)), q[b:b + 1]], axis=2)
+        of, lf = orc.attention(qf, k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.45, C)
+        assert np.array_equal(out[b], of[0, :, L - n_q:]) and np.array_equal(lse[b], lf[0, :, L - n_q:])
+
+
+def pin_decode_single_query_sees_whole_cache(orc):
+    """One new query attends to every cached key: the same as key padding with len."""
+    q, k, v = _rand(31, 2, 2, 1, 9, 4, 3)
+    lens = np.array([9, 5], np.int32)
+    o1, l1 = orc.attention(q, k, v, 0.5, DEC, lens)
+    o2, l2 = orc.attention(q, k, v, 0.5, P, lens)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def pin_decode_short_cache(orc):
+    """Queries whose position is negative (cache shorter than n_q) have no legal key."""
+    q, k, v = _rand(32, 1, 1, 3, 6, 2, 2)
+    out, lse = orc.attention(q, k, v, 0.5, DEC, np.array([2], np.int32))
+    assert np.all(out[0, 0, 0] == 0.0) and np.isneginf(lse[0, 0, 0])
+    assert np.all(np.isfinite(lse[0, 0, 1:]))
+    o1, _ = orc.attention(q[:, :, 1:2], k[:, :, :1], v[:, :, :1], 0.5)
+    assert np.array_equal(out[0, 0, 1], o1[0, 0, 0])
+
+
+def pin_decode_matrix_form(orc):
+    """Loop form equals the matrix form for the decode mask, with the lengths the decode
+    workloads use (one and several new queries, ragged caches)."""
+    for seed, n_q in ((33, 1), (34, 5)):
+        q, k, v = _rand(seed, 3, 2, n_q, 12, 4, 4)
+        lens = np.array([12, 6, n_q], np.int32)
+        out, lse = orc.attention(q, k, v, 0.3, DEC, lens)
+        om, lm, A = oracle.attention_matrix_form(q, k, v, 0.3, DEC, lens)
+        assert np.abs(out - om).max() < 1e-12 and np.abs(lse - lm).max() < 1e-12
+        w = orc.attention_weights(q, k, 0.3, DEC, lens)
+        assert np.abs(w - A).max() < 1e-12
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

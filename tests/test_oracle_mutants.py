@@ -34,6 +34,8 @@ MUTANTS = {
                       "long long voff = (long long)(bh / p->H) * p->n_k * p->d_v;"),
     "q_row_reversed": ("((long long)bh * p->n_q + i) * p->d_k", "((long long)bh * p->n_q + (p->n_q - 1 - i)) * p->d_k"),
     "bf16_widening": ("<< 16;", "<< 15;"),
+    "decode_off_by_one": ("j > p->key_lens[b] - p->n_q + i", "j >= p->key_lens[b] - p->n_q + i"),
+    "decode_start_aligned": ("j > p->key_lens[b] - p->n_q + i", "j > i"),
 }
 
 _CHILD = r"""
