@@ -51,7 +51,7 @@ NCU_TRAFFIC = {
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn_fwd_tc.cu", "ptx_sm103.cuh"):
+    for f in ("attn_fwd_tc.cu", "attn_decode.cu", "ptx_sm103.cuh"):
         with open(os.path.join(ROOT, "transformer_scaled_dot_mha_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -95,7 +95,7 @@ def weak_scaling_tflops(flops_per_rank_step: float, steps: int, max_total_ms: fl
 
 
 def mask_name(mode):
-    return {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[mode]
+    return {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding", 4: "decode"}[mode]
 
 
 def config_of(w, extra=None):
@@ -225,9 +225,16 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     key_lens = kld if w.mask_mode & W.MASK_KEY_PADDING else None
+    decode = bool(w.mask_mode & W.MASK_DECODE)
+    if decode:
+        ws = torch.empty(attn.attn_decode_workspace_size(w.B, w.H, w.n_q, w.n_k, w.d_k), dtype=torch.uint8,
+                         device=dev)
 
     def step():
-        attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens, stream)
+        if decode:
+            attn.attn_decode(qd, kd, vd, out, kld, ws, lse, w.scale, stream)
+        else:
+            attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -273,10 +280,21 @@ def run_ours(args, w):
     if rank != 0:
         return None
     peaks, peak_src = load_peaks()
-    achieved = flops_step / (ms_per_step / 1e3) / 1e12
-    peak = float(peaks["bf16_tflops"])
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((w.name, src_hash))
+    if decode:  # HBM-bound: one read of the used cache rows dominates
+        roof = {"bound": "hbm", "achieved": round(w.algorithmic_bytes(kl) / (ms_per_step / 1e3) / 1e9, 1),
+                "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "algorithmic_bytes": w.algorithmic_bytes(kl), "peak_source": f"hbm_gbs of {peak_src}",
+                "kernel": "attn_decode (split kernel + merge kernel, timed together)"}
+    else:
+        achieved = flops_step / (ms_per_step / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": float(peaks["bf16_tflops"]),
+                "unit": "TFLOP/s", "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                "kernel": "attn_fwd_tc_kernel"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = traffic
+    roof["kernel_source"] = src_hash
     line = {
         "metric": "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -286,12 +304,9 @@ def run_ours(args, w):
                                 "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
                                 "dense_equivalent_tflops": round(world * w.dense_flops() * args.steps /
                                                                  (total_ms / 1e3) / 1e12, 2)}),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"bf16_tflops (burst) of {peak_src}", "kernel": "attn_fwd_tc_kernel",
-                     "kernel_source": src_hash},
+        "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if decode else 1),
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -312,16 +327,28 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world):
     qd, kd, vd = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
     kld = torch.empty_like(klh, device=dev)
     out = torch.empty_like(outh, device=dev)
-    use_kl = bool(w.mask_mode & W.MASK_KEY_PADDING)
+    decode = bool(w.mask_mode & W.MASK_DECODE)
+    use_kl = bool(w.mask_mode & (W.MASK_KEY_PADDING | W.MASK_DECODE))
     steps = max(3, min(args.steps, 50))
+    if decode:
+        # a serving step: the key/value cache stays resident in HBM; the new queries
+        # and the cache lengths come from the host, the output goes back
+        kd.copy_(kh)
+        vd.copy_(vh)
+        ws = torch.empty(attn.attn_decode_workspace_size(w.B, w.H, w.n_q, w.n_k, w.d_k), dtype=torch.uint8,
+                         device=dev)
 
     def step():
         qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
+        if not decode:
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
         if use_kl:
             kld.copy_(klh, non_blocking=True)
-        attn.attn_fwd(qd, kd, vd, out, None, w.scale, w.mask_mode, kld if use_kl else None, stream)
+        if decode:
+            attn.attn_decode(qd, kd, vd, out, kld, ws, None, w.scale, stream)
+        else:
+            attn.attn_fwd(qd, kd, vd, out, None, w.scale, w.mask_mode, kld if use_kl else None, stream)
         outh.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -334,11 +361,15 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (klh.numel() * 4 if use_kl else 0)
+    h2d = sum(t.numel() * t.element_size() for t in ((qh,) if decode else (qh, kh, vh))) + \
+        (klh.numel() * 4 if use_kl else 0)
     d2h = outh.numel() * outh.element_size()
+    how = "pinned host buffers, copies and kernel on one stream, CUDA events"
+    if decode:
+        how += "; key/value cache resident on the device"
     return {"value": round(weak_scaling_tflops(flops_step, 1, ms, world), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
-            "steps": steps, "how": "pinned host buffers, copies and kernel on one stream, CUDA events"}
+            "steps": steps, "how": how}
 
 
 # ---------------------------------------------------------------- reference arm

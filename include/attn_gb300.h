@@ -43,6 +43,7 @@
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -87,13 +88,46 @@ int attn_fwd_f32(const float* q, const float* k, const float* v, float* out, flo
                  int mask_mode, const int32_t* key_lens, void* stream);
 
 /*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode needs for
+ * this shape (the split-K partial results: fp32 partial outputs, running maxima
+ * and sums). Returns 0 for an invalid shape. Depends only on the arguments.
+ */
+size_t attn_decode_workspace_size(int B, int h, int n_q, int n_max, int d);
+
+/*
+ * attn_decode -- one autoregressive decoding step against a key/value cache:
+ * n_q new queries per (b, h) attend to the cached keys up to their own position.
+ * Generation proceeds one position at a time under the causal mask of decoder
+ * self-attention (attention-paper-guide section 05; rockcohen.cc sections 5.3,
+ * 6.3); query i of batch b sits at position cache_lens[b] - n_q + i and key j is
+ * legal iff j <= cache_lens[b] - n_q + i. The result equals the last n_q rows of
+ * causal self-attention over the first cache_lens[b] positions.
+ *   q       bf16 [B, h, n_q, d]         k_cache, v_cache  bf16 [B, h, n_max, d]
+ *   out     bf16 [B, h, n_q, d]         lse  float [B, h, n_q] or NULL
+ *   cache_lens  int32 [B], device, each in [0, n_max] (a value outside is clamped to
+ *           that range before the query positions are placed). A query whose
+ *           position is negative (cache_lens[b] < n_q) has no legal key: out = 0,
+ *           lse = -inf.
+ *   workspace   device scratch of at least attn_decode_workspace_size(...) bytes,
+ *           16-byte aligned, owned by the caller; its contents on entry do not
+ *           matter and on return are undefined. Two calls that run at the same time
+ *           must not share a workspace.
+ * Supported: 1 <= n_q <= 16, d in {64, 128}, B*h <= 65535. Pointers 16-byte
+ * aligned. fp32 arithmetic throughout (scores, exp2, sums, P.V); the output is
+ * rounded to bf16 once. Asynchronous on `stream`; two kernels are launched.
+ */
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                int B, int h, int n_q, int n_max, int d, float scale,
+                const int32_t* cache_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_fault_status -- synchronises `stream`, then reports whether any kernel of
  * this library on the current device gave up waiting on one of its internal
  * barriers since the last clear (each such wait is bounded in time; a kernel that
  * gives up writes no further output and returns). Returns ATTN_OK,
  * ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA. If `clear` is non-zero the record is reset.
  * `fault_code` (may be NULL) receives the raw record: bit 0 producer, bit 1 MMA
- * issuer, bit 2 softmax, bit 3 epilogue.
+ * issuer, bit 2 softmax, bit 3 epilogue (attn_fwd), bit 4 decode copy (attn_decode).
  */
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code);
 

@@ -92,3 +92,27 @@ def test_library_has_no_oracle_dependency():
     for src in glob.glob(os.path.join(ROOT, "transformer_scaled_dot_mha_gb300", "**", "*.*"), recursive=True):
         if src.endswith((".py", ".cu", ".cuh", ".h")):
             assert "import oracle" not in open(src).read() and "attn_oracle" not in open(src).read(), src
+
+
+def test_decode_workspace_and_argument_checks(L):
+    ws = attn.attn_decode_workspace_size
+    assert ws(16, 16, 1, 8192, 64) > 0 and ws(16, 16, 1, 8192, 64) == ws(16, 16, 1, 8192, 64)
+    assert ws(1, 1, 17, 100, 64) == 0 and ws(1, 1, 1, 100, 96) == 0 and ws(0, 1, 1, 100, 64) == 0
+    need = ws(2, 3, 4, 500, 128)
+    f = L.attn_decode
+    ok = dict(q=16, k=32, v=48, out=64, lse=None, B=2, h=3, n_q=4, n_max=500, d=128, scale=0.088,
+              lens=80, ws=96, nbytes=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["h"], a["n_q"], a["n_max"], a["d"],
+                 a["scale"], a["lens"], a["ws"], a["nbytes"], None)
+    assert call(nbytes=need - 1) == attn.ATTN_ERR_INVALID      # workspace too small
+    assert call(ws=None) == attn.ATTN_ERR_INVALID
+    assert call(lens=None) == attn.ATTN_ERR_INVALID
+    assert call(ws=104) == attn.ATTN_ERR_INVALID               # misaligned workspace
+    assert call(q=24) == attn.ATTN_ERR_INVALID
+    assert call(n_q=0) == attn.ATTN_ERR_INVALID
+    assert call(n_q=17) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID

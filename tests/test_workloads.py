@@ -50,3 +50,16 @@ def test_legal_pairs_brute_force():
 def test_scale_is_float32_of_inverse_sqrt():
     assert W.default_scale(64) == 0.125
     assert W.default_scale(128) == float(np.float32(1 / np.sqrt(128.0)))
+
+
+def test_decode_legal_pairs_and_bytes():
+    w = W.WORKLOADS["decode_b16_h16_q1_k8192_d64"]
+    q, k, v, kl = W.make_inputs(w, B=3, H=2)
+    assert q.shape == (3, 2, 1, 64) and k.shape == (3, 2, 8192, 64)
+    assert np.all((kl >= 4096) & (kl <= 8192))
+    want = int(oracle.legal_mask(3, 1, 8192, oracle.MASK_DECODE, kl).sum()) * 2
+    assert W.legal_pairs(3, 2, 1, 8192, W.MASK_DECODE, kl) == want
+    kl2 = np.array([0, 2, 9], np.int32)
+    for n_q in (1, 3, 5):
+        want = int(oracle.legal_mask(3, n_q, 9, oracle.MASK_DECODE, kl2).sum())
+        assert W.legal_pairs(3, 1, n_q, 9, W.MASK_DECODE, kl2) == want

@@ -40,6 +40,10 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd.restype = i
         L.attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
         L.attn_fwd_f32.restype = i
+        L.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
+        L.attn_decode_workspace_size.restype = ctypes.c_size_t
+        L.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, ctypes.c_size_t, vp]
+        L.attn_decode.restype = i
         L.attn_fault_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint32)]
         L.attn_fault_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -110,6 +114,35 @@ def attention(q, k, v, scale=None, mask_mode=MASK_NONE, key_lens=None, with_lse=
     fn = attn_fwd if q.dtype == torch.bfloat16 else attn_fwd_f32
     fn(q, k, v, out, lse, scale, mask_mode, key_lens, stream)
     return (out, lse) if with_lse else out
+
+
+def attn_decode_workspace_size(B, H, n_q, n_max, d) -> int:
+    return int(lib().attn_decode_workspace_size(B, H, n_q, n_max, d))
+
+
+def attn_decode(q, k_cache, v_cache, out, cache_lens, workspace, lse=None, scale=None, stream=None):
+    """One decoding step: ``q [B,H,n_q,d]`` against caches ``[B,H,n_max,d]`` (bf16),
+    ``cache_lens`` int32 ``[B]``, caller-provided ``workspace`` (a CUDA uint8 tensor of
+    at least ``attn_decode_workspace_size`` bytes) and ``out`` (and optional ``lse``)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _check(t, n, torch.bfloat16)
+    B, H, n_q, d = q.shape
+    n_max = k_cache.shape[2]
+    if k_cache.shape != (B, H, n_max, d) or v_cache.shape != (B, H, n_max, d) or out.shape != q.shape:
+        raise ValueError("shape mismatch between q, caches and out")
+    _check(cache_lens, "cache_lens", torch.int32, 1)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 3)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, H, n_q, n_max, d,
+                           float(scale), _ptr(cache_lens), _ptr(workspace), nbytes, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode")
+    return out
 
 
 def attn_fault_status(stream=None, clear=True):

@@ -1,0 +1,407 @@
+// attn_decode.cu -- one autoregressive decoding step: n_q (1..16) new queries per
+// (batch, head) against a key/value cache, bf16 in and out, fp32 arithmetic.
+//
+// Query i of batch b sits at position cache_len[b] - n_q + i and attends to cache
+// keys 0..position: the causal mask of decoder self-attention applied to the newest
+// positions (generation proceeds one position at a time; attention-paper-guide
+// section 05, rockcohen.cc sections 5.3 and 6.3), with Eq. (1) softmax(QK^T/sqrt(d_k))V
+// per head (rockcohen.cc section 5.1).
+//
+// The work per query is tiny (a dot product and an axpy per cached key) while the
+// cache is large, so the step is bound by reading K and V from HBM once. Design:
+//   * split-K: the cache of each (b, h) is cut into `splits` ranges of whole
+//     128-key tiles, one CTA per (range, b*h), enough CTAs to fill every SM;
+//   * each CTA streams its 128-key K and V tiles with bulk asynchronous copies
+//     (cp.async.bulk, completion counted on an mbarrier) through a 3-stage ring,
+//     and runs the online softmax over its range in fp32: scores (thread = key),
+//     per-query max / exp2 / sum (warp per query), P.V (thread = value column
+//     pair x key part), with the running output rescaled when the maximum moves;
+//   * it writes its unnormalised partial output o, running maximum m and sum l to
+//     the workspace; a second kernel merges the ranges of each (b, h):
+//     o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, M = max_s m_s.
+// Waits on the copy barriers are bounded in time; a wait that runs out records a
+// fault bit (attn_fault_status) and the CTA stops after its copies have landed.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace attn {
+
+__device__ unsigned int g_decode_fault_word;  // fault record of the decode kernels
+
+namespace {
+
+constexpr int TK = 128;       // keys per tile
+constexpr int NTHREADS = 128;  // 4 warps
+constexpr int STAGES = 3;
+constexpr int MAX_NQ = 16;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr uint32_t FAULT_DECODE = 16;
+
+template <int D>
+struct DCfg {
+  static constexpr int ROW_BYTES = D * 2;
+  static constexpr int TILE_BYTES = TK * ROW_BYTES;  // one K or V tile
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
+  static constexpr int OFF_Q = OFF_V + STAGES * TILE_BYTES;    // float q_s[MAX_NQ][D]
+  static constexpr int OFF_S = OFF_Q + MAX_NQ * D * 4;         // float s_s[MAX_NQ][TK]
+  static constexpr int OFF_A = OFF_S + MAX_NQ * TK * 4;        // float alpha_s[MAX_NQ]
+  static constexpr int OFF_BAR = OFF_A + MAX_NQ * 4;           // uint64 full[STAGES]
+  static constexpr int SMEM_BYTES = OFF_BAR + STAGES * 8 + 16;
+  static constexpr int PARTS = NTHREADS / (D / 2);             // key parts in the P.V phase
+  static_assert(OFF_BAR % 8 == 0, "barrier alignment");
+};
+
+struct DecodeParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  uint16_t* out;
+  float* lse;
+  const int32_t* cache_lens;
+  float* ws_o;   // [BH][splits][n_q][D]
+  float* ws_ml;  // [BH][splits][n_q][2]
+  int H, n_q, n_max, splits;
+  float scale_log2;
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Tiles [t0, t1) of the cache range of this split.
+__device__ __forceinline__ void split_tiles(int len, int splits, int s, int& t0, int& t1) {
+  const int tiles = (len + TK - 1) / TK;
+  const int per = (tiles + splits - 1) / splits;
+  t0 = min(s * per, tiles);
+  t1 = min(t0 + per, tiles);
+}
+
+// NQ: compile-time bucket of the query count (n_q <= NQ), so that the per-query
+// loops are as long as needed and no longer.
+template <int D, int NQ>
+__global__ void __launch_bounds__(NTHREADS) attn_decode_split_kernel(const DecodeParams p) {
+  using C = DCfg<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t s_base = ptx::smem_u32(smem);
+  float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
+  float* s_s = reinterpret_cast<float*>(smem + C::OFF_S);
+  float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_A);
+  auto full = [&](int st) -> uint32_t { return s_base + C::OFF_BAR + 8u * st; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, bh = blockIdx.y, b = bh / p.H;
+  const int n_q = p.n_q;
+  const int len = min(max(p.cache_lens[b], 0), p.n_max);
+  int t_begin, t_end;
+  split_tiles(len, p.splits, split, t_begin, t_end);
+  const int n_tiles = t_end - t_begin;
+  const size_t cache_row0 = (size_t)bh * p.n_max;
+
+  if (tid == 0) {
+    for (int st = 0; st < STAGES; ++st) ptx::mbar_init(full(st), 1);
+    ptx::fence_mbar_init();
+  }
+  // queries, widened to fp32 (raw bf16 bits -> float)
+  for (int x = tid; x < n_q * D; x += NTHREADS) {
+    const uint32_t bits = (uint32_t)p.q[((size_t)bh * n_q) * D + x] << 16;
+    q_s[x] = __uint_as_float(bits);
+  }
+  __syncthreads();
+
+  auto issue = [&](int it) {  // copy tile t_begin + it into stage it % STAGES
+    const int tile = t_begin + it;
+    const int rows = min(TK, len - tile * TK);
+    const uint32_t bytes = (uint32_t)rows * C::ROW_BYTES;
+    const int st = it % STAGES;
+    ptx::mbar_arrive_expect_tx(full(st), 2 * bytes);
+    const size_t off = (cache_row0 + (size_t)tile * TK) * D;
+    bulk_load(s_base + C::OFF_K + st * C::TILE_BYTES, p.k + off, bytes, full(st));
+    bulk_load(s_base + C::OFF_V + st * C::TILE_BYTES, p.v + off, bytes, full(st));
+  };
+  if (tid == 0)
+    for (int it = 0; it < min(STAGES, n_tiles); ++it) issue(it);
+
+  // per-query running state, replicated over the lanes of the warp that owns the query
+  constexpr int QPW = (NQ + 3) / 4;  // queries per warp in the softmax phase
+  float m_run[QPW], l_run[QPW];
+#pragma unroll
+  for (int x = 0; x < QPW; ++x) {
+    m_run[x] = -INFINITY;
+    l_run[x] = 0.0f;
+  }
+  // P.V accumulators: this thread's value column pair, all queries, its key part
+  const int dp = tid % (D / 2), part = tid / (D / 2);
+  float2 acc[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) acc[q] = make_float2(0.0f, 0.0f);
+
+  bool ok = true;
+  int it_fail = 0;
+  for (int it = 0; it < n_tiles && ok; ++it) {
+    const int st = it % STAGES;
+    const int tile = t_begin + it;
+    const int rows = min(TK, len - tile * TK);
+    ok = __syncthreads_and(wait_full(full(st), (it / STAGES) & 1));
+    if (!ok) {
+      it_fail = it;
+      break;
+    }
+    const uint32_t* k_t = reinterpret_cast<const uint32_t*>(smem + C::OFF_K + st * C::TILE_BYTES);
+    const uint32_t* v_t = reinterpret_cast<const uint32_t*>(smem + C::OFF_V + st * C::TILE_BYTES);
+
+    // ---- scores: thread = key; word order rotated by the key to spread banks; two
+    // accumulator chains per query (even and odd value column)
+    {
+      const int kk = tid;
+      float dot0[NQ], dot1[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) dot0[q] = dot1[q] = 0.0f;
+      if (kk < rows) {
+#pragma unroll 4
+        for (int x = 0; x < D / 2; ++x) {
+          const int w = (x + kk) & (D / 2 - 1);
+          const uint32_t kw = k_t[kk * (D / 2) + w];
+          const float k0 = __uint_as_float(kw << 16), k1 = __uint_as_float(kw & 0xffff0000u);
+#pragma unroll
+          for (int q = 0; q < NQ; ++q)
+            if (q < n_q) {
+              const float2 qv = *reinterpret_cast<const float2*>(&q_s[q * D + 2 * w]);
+              dot0[q] = fmaf(qv.x, k0, dot0[q]);
+              dot1[q] = fmaf(qv.y, k1, dot1[q]);
+            }
+        }
+      }
+      const int j = tile * TK + kk;  // cache position of this key
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+        if (q < n_q)
+          s_s[q * TK + kk] = (kk < rows && j <= len - n_q + q) ? (dot0[q] + dot1[q]) * p.scale_log2 : -INFINITY;
+    }
+    __syncthreads();
+
+    // ---- online softmax: warp w owns queries w, w+4, w+8, w+12
+#pragma unroll
+    for (int x = 0; x < QPW; ++x) {
+      const int q = warp + 4 * x;
+      if (q < n_q) {
+        float sv[TK / 32];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int y = 0; y < TK / 32; ++y) {
+          sv[y] = s_s[q * TK + lane + 32 * y];
+          mt = fmaxf(mt, sv[y]);
+        }
+        mt = warp_max(mt);
+        const float m_new = fmaxf(m_run[x], mt);
+        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+        const float alpha = ptx::ex2(m_run[x] - m_use);  // 0 while nothing was legal
+        float ps = 0.0f;
+#pragma unroll
+        for (int y = 0; y < TK / 32; ++y) {
+          const float pv = ptx::ex2(sv[y] - m_use);
+          s_s[q * TK + lane + 32 * y] = pv;
+          ps += pv;
+        }
+        ps = warp_sum(ps);
+        l_run[x] = l_run[x] * alpha + ps;
+        m_run[x] = m_new;
+        if (lane == 0) alpha_s[q] = alpha;
+      }
+    }
+    __syncthreads();
+
+    // ---- P.V: thread = (value column pair dp, key part); keys of the part in order
+    {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+        if (q < n_q) {
+          const float a = alpha_s[q];
+          acc[q].x *= a;
+          acc[q].y *= a;
+        }
+      constexpr int KPP = TK / C::PARTS;  // keys per part
+      const int k_lo = part * KPP, k_hi = min(k_lo + KPP, rows);
+      for (int kk = k_lo; kk < k_hi; ++kk) {
+        const uint32_t vw = v_t[kk * (D / 2) + dp];
+        const float v0 = __uint_as_float(vw << 16), v1 = __uint_as_float(vw & 0xffff0000u);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (q < n_q) {
+            const float pv = s_s[q * TK + kk];
+            acc[q].x = fmaf(pv, v0, acc[q].x);
+            acc[q].y = fmaf(pv, v1, acc[q].y);
+          }
+      }
+    }
+    __syncthreads();  // stage `st` and s_s are free again
+    if (tid == 0 && it + STAGES < n_tiles) issue(it + STAGES);
+  }
+
+  if (!ok) {
+    // a copy never completed: record it, let the copies still in flight (tiles
+    // it_fail .. it_fail + STAGES - 1) land, then stop
+    if (tid == 0) {
+      atomicOr(&g_decode_fault_word, FAULT_DECODE);
+      for (int it = it_fail; it < min(it_fail + STAGES, n_tiles); ++it) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(full(it % STAGES), (it / STAGES) & 1))
+          if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) break;
+      }
+    }
+    __syncthreads();
+    return;
+  }
+
+  // ---- reduce the key parts through shared memory (the K ring is free), write partials
+  float* red = reinterpret_cast<float*>(smem + C::OFF_K);  // [PARTS][n_q][D]
+#pragma unroll
+  for (int q = 0; q < NQ; ++q)
+    if (q < n_q) *reinterpret_cast<float2*>(&red[(part * n_q + q) * D + 2 * dp]) = acc[q];
+  __syncthreads();
+  const size_t ws_row = ((size_t)bh * p.splits + split) * n_q;
+  for (int x = tid; x < n_q * D; x += NTHREADS) {
+    float o = 0.0f;
+#pragma unroll
+    for (int pp = 0; pp < C::PARTS; ++pp) o += red[pp * n_q * D + x];
+    p.ws_o[ws_row * D + x] = o;
+  }
+#pragma unroll
+  for (int x = 0; x < QPW; ++x) {
+    const int q = warp + 4 * x;
+    if (q < n_q && lane == 0) {
+      p.ws_ml[(ws_row + q) * 2 + 0] = m_run[x];
+      p.ws_ml[(ws_row + q) * 2 + 1] = l_run[x];
+    }
+  }
+}
+
+// Merge the split ranges of one (b, h): thread x handles output element x of n_q x D.
+template <int D>
+__global__ void __launch_bounds__(NTHREADS) attn_decode_combine_kernel(const DecodeParams p) {
+  const int bh = blockIdx.x;
+  const int n_q = p.n_q;
+  for (int x = threadIdx.x; x < n_q * D; x += NTHREADS) {
+    const int q = x / D;
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) {
+      const size_t r = ((size_t)bh * p.splits + s) * n_q + q;
+      if (p.ws_ml[r * 2 + 1] > 0.0f) M = fmaxf(M, p.ws_ml[r * 2]);
+    }
+    float L = 0.0f, o = 0.0f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < p.splits; ++s) {
+        const size_t r = ((size_t)bh * p.splits + s) * n_q + q;
+        const float l_s = p.ws_ml[r * 2 + 1];
+        if (l_s > 0.0f) {
+          const float w = ptx::ex2(p.ws_ml[r * 2] - M);
+          L = fmaf(w, l_s, L);
+          o = fmaf(w, p.ws_o[r * D + (x % D)], o);
+        }
+      }
+    }
+    const float res = (L > 0.0f) ? o / L : 0.0f;
+    p.out[((size_t)bh * n_q) * D + x] = __bfloat16_as_ushort(__float2bfloat16_rn(res));
+    if (p.lse && (x % D) == 0)
+      p.lse[(size_t)bh * n_q + q] = (L > 0.0f) ? (M + __log2f(L)) * 0.69314718055994530942f : -INFINITY;
+  }
+}
+
+template <int D>
+int launch_decode(const DecodeArgs& a, float* ws) {
+  using C = DCfg<D>;
+  void (*split_kernel)(const DecodeParams) = a.n_q <= 1   ? attn_decode_split_kernel<D, 1>
+                                             : a.n_q <= 2 ? attn_decode_split_kernel<D, 2>
+                                             : a.n_q <= 4 ? attn_decode_split_kernel<D, 4>
+                                             : a.n_q <= 8 ? attn_decode_split_kernel<D, 8>
+                                                          : attn_decode_split_kernel<D, 16>;
+  if (cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  DecodeParams p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.k = static_cast<const uint16_t*>(a.k);
+  p.v = static_cast<const uint16_t*>(a.v);
+  p.out = static_cast<uint16_t*>(a.out);
+  p.lse = a.lse;
+  p.cache_lens = a.cache_lens;
+  p.H = a.H;
+  p.n_q = a.n_q;
+  p.n_max = a.n_max;
+  p.splits = decode_splits(a.B, a.H, a.n_max);
+  p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
+  const long long bh = (long long)a.B * a.H;
+  if (bh > 65535) return ATTN_ERR_UNSUPPORTED;  // one grid row per (b, h)
+  p.ws_o = ws;
+  p.ws_ml = ws + (size_t)bh * p.splits * a.n_q * D;
+  dim3 grid(p.splits, (unsigned)bh);
+  split_kernel<<<grid, NTHREADS, C::SMEM_BYTES, a.stream>>>(p);
+  if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  attn_decode_combine_kernel<D><<<(unsigned)bh, NTHREADS, 0, a.stream>>>(p);
+  return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int decode_splits(int B, int H, int n_max) {
+  const long long bh = (long long)B * H;
+  const long long target = 4LL * 152;  // CTAs to cover every SM a few times
+  long long s = (target + bh - 1) / bh;
+  const long long tiles = (n_max + TK - 1) / TK;
+  if (s > tiles) s = tiles;
+  if (s > 64) s = 64;
+  return (int)(s < 1 ? 1 : s);
+}
+
+size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d) {
+  const size_t rows = (size_t)B * H * decode_splits(B, H, n_max) * n_q;
+  return rows * ((size_t)d + 2) * sizeof(float);
+}
+
+int read_decode_fault_word(int clear, uint32_t* out) {
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_decode_fault_word, sizeof w) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (clear) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_decode_fault_word, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  *out = w;
+  return ATTN_OK;
+}
+
+int launch_attn_decode(const DecodeArgs& a, void* workspace) {
+  float* ws = static_cast<float*>(workspace);
+  if (a.d == 64) return launch_decode<64>(a, ws);
+  if (a.d == 128) return launch_decode<128>(a, ws);
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace attn

@@ -591,6 +591,9 @@ int read_fault_word(cudaStream_t stream, int clear, uint32_t* out) {
     const uint32_t zero = 0;
     if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
   }
+  uint32_t wd = 0;
+  if (read_decode_fault_word(clear, &wd) != ATTN_OK) return ATTN_ERR_CUDA;
+  w |= wd;
   if (out) *out = w;
   return w ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }

@@ -43,8 +43,25 @@ struct F32Args {
   cudaStream_t stream;
 };
 
+// Validated arguments of one decode step.
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int B, H, n_q, n_max, d;
+  float scale;
+  const int32_t* cache_lens;
+  cudaStream_t stream;
+};
+
 int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc);   // attn_fwd_tc.cu
 int launch_attn_f32(const F32Args& a);                       // attn_fwd_f32.cu
 int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd_tc.cu
+int decode_splits(int B, int H, int n_max);                              // attn_decode.cu
+size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d);  // attn_decode.cu
+int launch_attn_decode(const DecodeArgs& a, void* workspace);            // attn_decode.cu
+int read_decode_fault_word(int clear, uint32_t* out);                   // attn_decode.cu
 
 }  // namespace attn

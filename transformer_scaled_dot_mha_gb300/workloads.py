@@ -8,8 +8,8 @@ Recipe (the same for every workload):
   * Q, K, V: standard normal float32 draws in that order, times ``input_scale``;
     bf16 workloads round them to bf16 with round-to-nearest-even (bit patterns
     kept as uint16); float32 workloads keep them as drawn;
-  * key lengths (key-padding workloads only): integers drawn uniformly from the
-    inclusive range ``key_len_range`` after V.
+  * key lengths (key-padding and decode workloads): integers drawn uniformly from
+    the inclusive range ``key_len_range`` after V (for decode, the cache length).
 
 Shapes follow the pages' base and big Transformer sizes (d_model 512 with h = 8,
 d_model 1024 with h = 16, so d_k = d_v = 64 per head; vlmlib.cn summary,
@@ -23,7 +23,7 @@ import math
 
 import numpy as np
 
-MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_DECODE = 0, 1, 2, 4
 SEED_BASE = 20170612
 
 
@@ -56,11 +56,23 @@ class Workload:
         return legal_pairs(self.B, self.H, self.n_q, self.n_k, self.mask_mode, key_lens)
 
     def algorithmic_flops(self, key_lens=None) -> float:
-        """2 (d_k + d_v) multiply-adds per legal pair: one QK^T dot and one P.V row."""
+        """2 (d_k + d_v) FLOPs per legal pair: a d_k-long dot product and a d_v-long axpy."""
         return 2.0 * (self.d_k + self.d_v) * self.legal_pairs(key_lens)
 
     def dense_flops(self) -> float:
         return 2.0 * (self.d_k + self.d_v) * self.B * self.H * self.n_q * self.n_k
+
+    def algorithmic_bytes(self, key_lens=None) -> float:
+        """Bytes a perfect kernel moves: Q, the K/V rows some query may use, O (bf16) and
+        lse (fp32), each once."""
+        rows_kv = 0
+        for b in range(self.B):
+            lim = self.n_k
+            if self.mask_mode & (MASK_KEY_PADDING | MASK_DECODE):
+                lim = min(lim, int(key_lens[b]))
+            rows_kv += lim
+        return float(self.H * (rows_kv * (self.d_k + self.d_v) * 2 +
+                               self.B * self.n_q * (self.d_k * 2 + self.d_v * 2 + 4)))
 
 
 def default_scale(d_k: int) -> float:
@@ -73,6 +85,11 @@ def legal_pairs(B, H, n_q, n_k, mask_mode, key_lens=None) -> int:
         lim = n_k
         if mask_mode & MASK_KEY_PADDING:
             lim = min(lim, int(key_lens[b]))
+        if mask_mode & MASK_DECODE:
+            # query i sits at position len - n_q + i and sees keys 0..position
+            L = min(int(key_lens[b]), n_k)
+            total += sum(max(0, L - n_q + i + 1) for i in range(n_q))
+            continue
         if mask_mode & MASK_CAUSAL:
             # query i sees keys 0..min(i, lim-1)
             full = min(n_q, lim)  # rows whose causal limit i+1 <= lim
@@ -95,6 +112,9 @@ WORKLOADS = {w.name: w for w in [
     _wl(5, "long_none_b2_h16_n8192_d64", 2, 16, 8192, 8192, 64, "bf16", MASK_NONE, None, 0.5),
     _wl(6, "long_causal_b2_h16_n8192_d128", 2, 16, 8192, 8192, 128, "bf16", MASK_CAUSAL, None, 0.5),
     _wl(7, "long_none_b2_h16_n8192_d128", 2, 16, 8192, 8192, 128, "bf16", MASK_NONE, None, 0.5),
+    # one autoregressive decoding step (one new query) against a key/value cache
+    _wl(8, "decode_b32_h8_q1_k2048_d64", 32, 8, 1, 2048, 64, "bf16", MASK_DECODE, (1024, 2048)),
+    _wl(9, "decode_b16_h16_q1_k8192_d64", 16, 16, 1, 8192, 64, "bf16", MASK_DECODE, (4096, 8192)),
 ]}
 
 
@@ -121,7 +141,7 @@ def make_inputs(w: Workload, seed: int | None = None, **shape):
         if w.input_scale != 1.0:
             x *= np.float32(w.input_scale)
         arrs.append(to_bf16_bits(x) if w.dtype == "bf16" else x)
-    if w.mask_mode & MASK_KEY_PADDING:
+    if w.mask_mode & (MASK_KEY_PADDING | MASK_DECODE):
         lo, hi = w.key_len_range
         lo, hi = min(lo, n_k), min(hi, n_k)
         key_lens = rng.integers(lo, hi, size=B, endpoint=True).astype(np.int32)
