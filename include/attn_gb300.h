@@ -121,6 +121,34 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
                 const int32_t* cache_lens, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device memory.
+ * (An addition of this library; the paper has no counterpart.)
+ * Some callers have no way to obtain device scratch: code running while its stream
+ * is being captured into a CUDA graph (an allocation is not a stream operation and
+ * may synchronise the device or be refused during capture), latency-critical
+ * serving loops that must not enter the allocator, and plug-ins whose host
+ * framework owns every device buffer. This entry point takes the same arguments as
+ * attn_decode minus the workspace and allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library call. Its scratch is a static buffer of
+ * ATTN_DECODE_NOALLOC_MAX_BYTES inside the library's device image, present on every
+ * GPU that loads the library until the process exits.
+ *   - The first call on a device looks up the buffer's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one buffer, which keeps the last call's
+ *     contents (the kernels write every slot before reading it, so nothing needs
+ *     clearing). Calls whose GPU work overlaps -- on different streams, or from
+ *     several host threads -- race on it: order them, e.g. on one stream.
+ *   - A shape whose workspace (attn_decode_workspace_size) exceeds
+ *     ATTN_DECODE_NOALLOC_MAX_BYTES returns ATTN_ERR_UNSUPPORTED and launches
+ *     nothing; use attn_decode with a caller workspace for it.
+ * Results are those of attn_decode on the same inputs.
+ */
+#define ATTN_DECODE_NOALLOC_MAX_BYTES (4u << 20)
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                        int B, int h, int n_q, int n_max, int d, float scale,
+                        const int32_t* cache_lens, void* stream);
+
+/*
  * attn_fault_status -- synchronises `stream`, then reports whether any kernel of
  * this library on the current device gave up waiting on one of its internal
  * barriers since the last clear (each such wait is bounded in time; a kernel that

@@ -44,6 +44,8 @@ def lib() -> ctypes.CDLL:
         L.attn_decode_workspace_size.restype = ctypes.c_size_t
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, ctypes.c_size_t, vp]
         L.attn_decode.restype = i
+        L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
+        L.attn_decode_noalloc.restype = i
         L.attn_fault_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint32)]
         L.attn_fault_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -142,6 +144,33 @@ def attn_decode(q, k_cache, v_cache, out, cache_lens, workspace, lse=None, scale
                            float(scale), _ptr(cache_lens), _ptr(workspace), nbytes, _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_decode")
+    return out
+
+
+NOALLOC_MAX_BYTES = 4 << 20  # ATTN_DECODE_NOALLOC_MAX_BYTES
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, out, cache_lens, lse=None, scale=None, stream=None):
+    """attn_decode without a workspace argument, for callers that cannot allocate
+    device memory (e.g. while capturing a CUDA graph): the library uses its own
+    static device buffer of NOALLOC_MAX_BYTES, shared by every call on the device,
+    so calls must not overlap on the GPU. The first call on a device does a
+    one-time set-up and should come before any stream capture."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _check(t, n, torch.bfloat16)
+    B, H, n_q, d = q.shape
+    n_max = k_cache.shape[2]
+    if k_cache.shape != (B, H, n_max, d) or v_cache.shape != (B, H, n_max, d) or out.shape != q.shape:
+        raise ValueError("shape mismatch between q, caches and out")
+    _check(cache_lens, "cache_lens", torch.int32, 1)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 3)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, H, n_q, n_max,
+                                   d, float(scale), _ptr(cache_lens), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode_noalloc")
     return out
 
 

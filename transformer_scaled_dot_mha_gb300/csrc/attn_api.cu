@@ -95,6 +95,21 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
   return attn::launch_attn_decode(a, workspace);
 }
 
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse, int B,
+                        int h, int n_q, int n_max, int d, float scale, const int32_t* cache_lens, void* stream) {
+  if (!q || !k_cache || !v_cache || !out || !cache_lens) return ATTN_ERR_INVALID;
+  if (B <= 0 || h <= 0 || n_q <= 0 || n_max <= 0 || d <= 0) return ATTN_ERR_INVALID;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(cache_lens, 4) || (lse && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID;
+  if (n_q > 16 || (d != 64 && d != 128) || (long long)B * h > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * h * n_max > (1LL << 40) / d) return ATTN_ERR_INVALID;
+  attn::DecodeArgs a{q, k_cache, v_cache, out, lse, B, h, n_q, n_max, d, scale, cache_lens,
+                     static_cast<cudaStream_t>(stream)};
+  return attn::launch_attn_decode_noalloc(a);
+}
+
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code) {
   return attn::read_fault_word(static_cast<cudaStream_t>(stream), clear, fault_code);
 }

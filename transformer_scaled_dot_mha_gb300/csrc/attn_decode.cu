@@ -26,6 +26,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "attn_internal.h"
 #include "ptx_sm103.cuh"
@@ -33,6 +34,12 @@
 namespace attn {
 
 __device__ unsigned int g_decode_fault_word;  // fault record of the decode kernels
+
+// Scratch of attn_decode_noalloc: a fixed buffer in the library's own device
+// memory, one per device that loads the library, kept until the process exits.
+// Host code must not use the symbol itself as an address; it looks the device
+// address up once per device (decode_noalloc_scratch below).
+static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_DECODE_NOALLOC_MAX_BYTES];
 
 namespace {
 
@@ -395,6 +402,35 @@ int read_decode_fault_word(int clear, uint32_t* out) {
   }
   *out = w;
   return ATTN_OK;
+}
+
+namespace {
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[64];  // device address of g_decode_scratch, per device, once looked up
+}  // namespace
+
+// Device address of the static scratch on the current device; the first call on a
+// device looks it up (cudaGetSymbolAddress) with that device current.
+static int decode_noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return ATTN_ERR_CUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
+int launch_attn_decode_noalloc(const DecodeArgs& a) {
+  if (decode_workspace_bytes(a.B, a.H, a.n_q, a.n_max, a.d) > sizeof(g_decode_scratch)) return ATTN_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const int st = decode_noalloc_scratch(&scratch);
+  if (st != ATTN_OK) return st;
+  // every slot the kernels read is written first in the same call: nothing to clear
+  return launch_attn_decode(a, scratch);
 }
 
 int launch_attn_decode(const DecodeArgs& a, void* workspace) {

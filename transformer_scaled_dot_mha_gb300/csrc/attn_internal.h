@@ -62,6 +62,7 @@ int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd
 int decode_splits(int B, int H, int n_max);                              // attn_decode.cu
 size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d);  // attn_decode.cu
 int launch_attn_decode(const DecodeArgs& a, void* workspace);            // attn_decode.cu
+int launch_attn_decode_noalloc(const DecodeArgs& a);                     // attn_decode.cu
 int read_decode_fault_word(int clear, uint32_t* out);                   // attn_decode.cu
 
 }  // namespace attn
