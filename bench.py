@@ -45,7 +45,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel sources it was measured on; reported only while the sources match.
 NCU_TRAFFIC = {
     # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
-    ("long_causal_b2_h16_n8192_d64", "d94749fd0342898a"): 143211776,
+    ("long_causal_b2_h16_n8192_d64", "4eb5bc9770d38463"): 143104512,
+    # profiles/attn_decode_split_kernel_decode_b16_h16_q1_k8192_d64.md (split kernel only)
+    ("decode_b16_h16_q1_k8192_d64", "4eb5bc9770d38463"): 424460032,
 }
 
 
