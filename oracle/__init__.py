@@ -29,7 +29,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "attn_oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
-MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_DECODE = 0, 1, 2, 4
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_DECODE, MASK_WINDOW = 0, 1, 2, 4, 8
 _DTYPES = {np.dtype(np.float64): 0, np.dtype(np.float32): 1, np.dtype(np.uint16): 2}
 _CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
 
@@ -57,9 +57,9 @@ class Oracle:
             raise FileNotFoundError(f"oracle library {path} is not built; call oracle.build()")
         self.lib = ctypes.CDLL(path)
         vp, i, d, lp = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_longlong
-        self.lib.oracle_attn.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, vp, vp, i]
-        self.lib.oracle_attn_rows.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, lp, vp, vp, vp, i]
-        self.lib.oracle_attn_weights.argtypes = [vp, vp, i, i, i, i, i, i, d, i, vp, vp]
+        self.lib.oracle_attn.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, vp, vp, i]
+        self.lib.oracle_attn_rows.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, lp, vp, vp, vp, i]
+        self.lib.oracle_attn_weights.argtypes = [vp, vp, i, i, i, i, i, i, d, i, vp, i, vp]
         for f in (self.lib.oracle_attn, self.lib.oracle_attn_rows, self.lib.oracle_attn_weights):
             f.restype = ctypes.c_int
 
@@ -86,7 +86,7 @@ class Oracle:
     def _threads(n_threads):
         return int(n_threads) if n_threads else (os.cpu_count() or 1)
 
-    def attention(self, q, k, v, scale, mask_mode=MASK_NONE, key_lens=None, n_threads=None):
+    def attention(self, q, k, v, scale, mask_mode=MASK_NONE, key_lens=None, n_threads=None, window=0):
         """Full output ``O [B,H,n_q,d_v]`` and ``lse [B,H,n_q]`` in float64."""
         (q, k, v), dt = self._inputs(q, k, v)
         B, H, n_q, d_k = q.shape
@@ -96,12 +96,12 @@ class Oracle:
         lse = np.empty((B, H, n_q), np.float64)
         rc = self.lib.oracle_attn(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt, B, H, n_q, n_k, d_k, d_v,
                                   float(scale), int(mask_mode), kl.ctypes.data if kl is not None else None,
-                                  out.ctypes.data, lse.ctypes.data, self._threads(n_threads))
+                                  int(window), out.ctypes.data, lse.ctypes.data, self._threads(n_threads))
         if rc != 0:
             raise ValueError("oracle_attn rejected its arguments")
         return out, lse
 
-    def attention_rows(self, q, k, v, scale, row_ids, mask_mode=MASK_NONE, key_lens=None, n_threads=None):
+    def attention_rows(self, q, k, v, scale, row_ids, mask_mode=MASK_NONE, key_lens=None, n_threads=None, window=0):
         """Output rows for flat row ids ``(b*H + h)*n_q + i``: ``(out [R,d_v], lse [R])``."""
         (q, k, v), dt = self._inputs(q, k, v)
         B, H, n_q, d_k = q.shape
@@ -112,13 +112,13 @@ class Oracle:
         lse = np.empty((ids.size,), np.float64)
         rc = self.lib.oracle_attn_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dt, B, H, n_q, n_k, d_k, d_v,
                                        float(scale), int(mask_mode), kl.ctypes.data if kl is not None else None,
-                                       ids.size, ids.ctypes.data, out.ctypes.data, lse.ctypes.data,
+                                       int(window), ids.size, ids.ctypes.data, out.ctypes.data, lse.ctypes.data,
                                        self._threads(n_threads))
         if rc != 0:
             raise ValueError("oracle_attn_rows rejected its arguments")
         return out, lse
 
-    def attention_weights(self, q, k, scale, mask_mode=MASK_NONE, key_lens=None):
+    def attention_weights(self, q, k, scale, mask_mode=MASK_NONE, key_lens=None, window=0):
         """The softmax weight matrix ``A [B,H,n_q,n_k]`` (illegal entries exactly 0)."""
         (q, k), dt = self._inputs(q, k, None)
         B, H, n_q, d_k = q.shape
@@ -126,13 +126,14 @@ class Oracle:
         kl = self._lens(mask_mode, key_lens, B)
         w = np.empty((B, H, n_q, n_k), np.float64)
         rc = self.lib.oracle_attn_weights(q.ctypes.data, k.ctypes.data, dt, B, H, n_q, n_k, d_k, float(scale),
-                                          int(mask_mode), kl.ctypes.data if kl is not None else None, w.ctypes.data)
+                                          int(mask_mode), kl.ctypes.data if kl is not None else None, int(window),
+                                          w.ctypes.data)
         if rc != 0:
             raise ValueError("oracle_attn_weights rejected its arguments")
         return w
 
 
-def legal_mask(B, n_q, n_k, mask_mode, key_lens=None) -> np.ndarray:
+def legal_mask(B, n_q, n_k, mask_mode, key_lens=None, window=0) -> np.ndarray:
     """Boolean [B,1,n_q,n_k]: True where key j is a legal connection for query i."""
     i = np.arange(n_q)[:, None]
     j = np.arange(n_k)[None, :]
@@ -144,10 +145,12 @@ def legal_mask(B, n_q, n_k, mask_mode, key_lens=None) -> np.ndarray:
     if mask_mode & MASK_DECODE:  # query i sits at position key_len - n_q + i
         pos = np.asarray(key_lens).reshape(B, 1, 1, 1) - n_q + i[None, None]
         ok &= (j[None, None] <= pos)
+    if mask_mode & MASK_WINDOW:  # neighbourhood of radius `window`
+        ok &= (np.abs(i - j) <= window)[None, None]
     return ok
 
 
-def attention_matrix_form(q, k, v, scale, mask_mode=MASK_NONE, key_lens=None):
+def attention_matrix_form(q, k, v, scale, mask_mode=MASK_NONE, key_lens=None, window=0):
     """Matrix form of Eq. (1) in float64 with numpy/scipy library steps.
 
     S = scale * Q K^T; S = -inf where illegal; A = row softmax(S); O = A V;
@@ -159,7 +162,7 @@ def attention_matrix_form(q, k, v, scale, mask_mode=MASK_NONE, key_lens=None):
     B, H, n_q, _ = q.shape
     n_k = k.shape[2]
     S = scale * (q @ np.swapaxes(k, -1, -2))
-    S = np.where(legal_mask(B, n_q, n_k, mask_mode, key_lens), S, -np.inf)
+    S = np.where(legal_mask(B, n_q, n_k, mask_mode, key_lens, window), S, -np.inf)
     empty = np.all(np.isneginf(S), axis=-1)
     S_safe = np.where(empty[..., None], 0.0, S)
     A = np.where(empty[..., None], 0.0, softmax(S_safe, axis=-1))

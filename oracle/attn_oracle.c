@@ -42,6 +42,7 @@ typedef struct {
   double scale;
   int mask_mode;
   const int* key_lens;
+  int window;
 } problem;
 
 /* Element idx of an input array, widened exactly to double. */
@@ -60,6 +61,7 @@ static int legal(const problem* p, int b, int i, int j) {
   if ((p->mask_mode & ORACLE_MASK_CAUSAL) && j > i) return 0;
   if ((p->mask_mode & ORACLE_MASK_KEY_PADDING) && j >= p->key_lens[b]) return 0;
   if ((p->mask_mode & ORACLE_MASK_DECODE) && j > p->key_lens[b] - p->n_q + i) return 0;
+  if ((p->mask_mode & ORACLE_MASK_WINDOW) && (j > i + p->window || j < i - p->window)) return 0;
   return 1;
 }
 
@@ -144,7 +146,10 @@ static int check(const problem* p) {
   if (!p->q || !p->k) return -1;
   if (p->dtype < ORACLE_F64 || p->dtype > ORACLE_BF16) return -1;
   if (p->B <= 0 || p->H <= 0 || p->n_q <= 0 || p->n_k <= 0 || p->d_k <= 0 || p->d_v < 0) return -1;
-  if ((p->mask_mode & ~(ORACLE_MASK_CAUSAL | ORACLE_MASK_KEY_PADDING | ORACLE_MASK_DECODE)) != 0) return -1;
+  if ((p->mask_mode & ~(ORACLE_MASK_CAUSAL | ORACLE_MASK_KEY_PADDING | ORACLE_MASK_DECODE | ORACLE_MASK_WINDOW)) != 0)
+    return -1;
+  if ((p->mask_mode & ORACLE_MASK_DECODE) && (p->mask_mode & ORACLE_MASK_WINDOW)) return -1;
+  if ((p->mask_mode & ORACLE_MASK_WINDOW) && p->window < 0) return -1;
   if ((p->mask_mode & ORACLE_MASK_CAUSAL) && (p->mask_mode & ORACLE_MASK_DECODE)) return -1;
   if ((p->mask_mode & (ORACLE_MASK_KEY_PADDING | ORACLE_MASK_DECODE)) && !p->key_lens) return -1;
   return 0;
@@ -182,24 +187,25 @@ static int run(const problem* p, long long n_rows, const long long* row_ids, dou
 }
 
 int oracle_attn(const void* q, const void* k, const void* v, int dtype, int B, int H, int n_q, int n_k,
-                int d_k, int d_v, double scale, int mask_mode, const int* key_lens, double* out, double* lse,
-                int n_threads) {
-  problem p = {q, k, v, dtype, B, H, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens};
+                int d_k, int d_v, double scale, int mask_mode, const int* key_lens, int window, double* out,
+                double* lse, int n_threads) {
+  problem p = {q, k, v, dtype, B, H, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens, window};
   if (check(&p) != 0 || !v || !out) return -1;
   return run(&p, (long long)B * H * n_q, NULL, out, lse, n_threads);
 }
 
 int oracle_attn_rows(const void* q, const void* k, const void* v, int dtype, int B, int H, int n_q, int n_k,
-                     int d_k, int d_v, double scale, int mask_mode, const int* key_lens, long long n_rows,
-                     const long long* row_ids, double* out_rows, double* lse_rows, int n_threads) {
-  problem p = {q, k, v, dtype, B, H, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens};
+                     int d_k, int d_v, double scale, int mask_mode, const int* key_lens, int window,
+                     long long n_rows, const long long* row_ids, double* out_rows, double* lse_rows,
+                     int n_threads) {
+  problem p = {q, k, v, dtype, B, H, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens, window};
   if (check(&p) != 0 || !v || !out_rows || !row_ids || n_rows < 0) return -1;
   return run(&p, n_rows, row_ids, out_rows, lse_rows, n_threads);
 }
 
 int oracle_attn_weights(const void* q, const void* k, int dtype, int B, int H, int n_q, int n_k, int d_k,
-                        double scale, int mask_mode, const int* key_lens, double* weights) {
-  problem p = {q, k, NULL, dtype, B, H, n_q, n_k, d_k, 0, scale, mask_mode, key_lens};
+                        double scale, int mask_mode, const int* key_lens, int window, double* weights) {
+  problem p = {q, k, NULL, dtype, B, H, n_q, n_k, d_k, 0, scale, mask_mode, key_lens, window};
   if (check(&p) != 0 || !weights) return -1;
   for (int bh = 0; bh < B * H; ++bh)
     for (int i = 0; i < n_q; ++i) {

@@ -21,6 +21,9 @@
  *   of decoder self-attention applied to the newest n_q positions (attention-paper-
  *   guide section 05 and rockcohen.cc section 6.3: generation proceeds one position
  *   at a time and each position sees only positions up to itself).
+ *   Local window (restricted self-attention, the pages' long-sequence proposal:
+ *   attend only to positions within a neighbourhood r, cost O(r n d); csdn blog
+ *   section 4.3, vlmlib.cn "limitations"): key j is illegal when |i - j| > window.
  *
  * Conventions chosen where the pages are silent:
  *   - a row with no legal key returns o = 0 and lse = -inf;
@@ -40,22 +43,23 @@ extern "C" {
 /* element type of the Q/K/V input arrays */
 enum { ORACLE_F64 = 0, ORACLE_F32 = 1, ORACLE_BF16 = 2 /* raw bf16 bit patterns, uint16 */ };
 /* mask bits */
-enum { ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_KEY_PADDING = 2, ORACLE_MASK_DECODE = 4 };
+enum { ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_KEY_PADDING = 2, ORACLE_MASK_DECODE = 4, ORACLE_MASK_WINDOW = 8 };
 
 /* Full output. out: B*H*n_q*d_v doubles; lse: B*H*n_q doubles or NULL.
  * key_lens: B ints, required iff mask bit 2 or 4 is set. Bits 1 and 4 are exclusive.
+ * window: radius of mask bit 8 (>= 0), ignored otherwise; bits 4 and 8 are exclusive.
  * n_threads <= 0 means 1.
  * Returns 0, or -1 on an invalid argument. */
 int oracle_attn(const void* q, const void* k, const void* v, int dtype,
                 int B, int H, int n_q, int n_k, int d_k, int d_v, double scale,
-                int mask_mode, const int* key_lens,
+                int mask_mode, const int* key_lens, int window,
                 double* out, double* lse, int n_threads);
 
 /* A subset of query rows. row_ids[r] = (b*H + h)*n_q + i. out_rows: n_rows*d_v,
  * lse_rows: n_rows (or NULL). Same semantics as oracle_attn for those rows. */
 int oracle_attn_rows(const void* q, const void* k, const void* v, int dtype,
                      int B, int H, int n_q, int n_k, int d_k, int d_v, double scale,
-                     int mask_mode, const int* key_lens,
+                     int mask_mode, const int* key_lens, int window,
                      long long n_rows, const long long* row_ids,
                      double* out_rows, double* lse_rows, int n_threads);
 
@@ -63,7 +67,7 @@ int oracle_attn_rows(const void* q, const void* k, const void* v, int dtype,
  * Illegal entries are exactly 0.0; a row with no legal key is all zeros. */
 int oracle_attn_weights(const void* q, const void* k, int dtype,
                         int B, int H, int n_q, int n_k, int d_k, double scale,
-                        int mask_mode, const int* key_lens, double* weights);
+                        int mask_mode, const int* key_lens, int window, double* weights);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,7 @@ import numpy as np
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-C, P, DEC = oracle.MASK_CAUSAL, oracle.MASK_KEY_PADDING, oracle.MASK_DECODE
+C, P, DEC, WIN = oracle.MASK_CAUSAL, oracle.MASK_KEY_PADDING, oracle.MASK_DECODE, oracle.MASK_WINDOW
 
 
 def _golden(name):
@@ -324,6 +324,51 @@ def pin_decode_matrix_form(orc):
         assert np.abs(out - om).max() < 1e-12 and np.abs(lse - lm).max() < 1e-12
         w = orc.attention_weights(q, k, 0.3, DEC, lens)
         assert np.abs(w - A).max() < 1e-12
+
+
+# ---------------------------------------------------------------- local window (restricted self-attention)
+def pin_window_is_neighbourhood_attention(orc):
+    """Restricted self-attention (csdn blog section 4.3; vlmlib.cn "limitations"): row i
+    attends to keys i-r..i+r only, i.e. equals unmasked attention over that slice;
+    with the causal mask, to keys i-r..i. Brute force row by row, with key padding."""
+    q, k, v = _rand(40, 2, 2, 9, 9, 3, 4)
+    kl = np.array([9, 6], np.int32)
+    for r in (0, 1, 3, 20):
+        for mode in (WIN, WIN | C, WIN | P, WIN | C | P):
+            out, lse = orc.attention(q, k, v, 0.4, mode, kl, window=r)
+            for b in range(2):
+                for i in range(9):
+                    lo = max(0, i - r)
+                    hi = min(i + r + 1, 9)
+                    if mode & C:
+                        hi = min(hi, i + 1)
+                    if mode & P:
+                        hi = min(hi, kl[b])
+                    if hi <= lo:
+                        assert np.all(out[b, :, i] == 0.0) and np.all(np.isneginf(lse[b, :, i]))
+                        continue
+                    o1, l1 = orc.attention(q[b:b + 1, :, i:i + 1], k[b:b + 1, :, lo:hi], v[b:b + 1, :, lo:hi], 0.4)
+                    assert np.array_equal(out[b, :, i], o1[0, :, 0]) and np.array_equal(lse[b, :, i], l1[0, :, 0])
+
+
+def pin_window_limits(orc):
+    """A window covering the whole sequence changes nothing; radius 0 returns V[i]."""
+    q, k, v = _rand(41, 1, 2, 7, 7, 4, 3)
+    o_all, l_all = orc.attention(q, k, v, 0.5, C)
+    o_w, l_w = orc.attention(q, k, v, 0.5, C | WIN, window=7)
+    assert np.array_equal(o_all, o_w) and np.array_equal(l_all, l_w)
+    o0, _ = orc.attention(q, k, v, 0.5, WIN, window=0)
+    assert np.array_equal(o0, v)
+
+
+def pin_window_matrix_form(orc):
+    q, k, v = _rand(42, 2, 2, 11, 11, 4, 4)
+    kl = np.array([11, 8], np.int32)
+    for mode, r in ((WIN, 2), (WIN | C, 4), (WIN | P, 3)):
+        out, lse = orc.attention(q, k, v, 0.3, mode, kl, window=r)
+        om, lm, A = oracle.attention_matrix_form(q, k, v, 0.3, mode, kl, window=r)
+        assert np.abs(out - om).max() < 1e-12 and np.abs(lse - lm).max() < 1e-12
+        assert np.abs(orc.attention_weights(q, k, 0.3, mode, kl, window=r) - A).max() < 1e-12
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -36,6 +36,8 @@ MUTANTS = {
     "bf16_widening": ("<< 16;", "<< 15;"),
     "decode_off_by_one": ("j > p->key_lens[b] - p->n_q + i", "j >= p->key_lens[b] - p->n_q + i"),
     "decode_start_aligned": ("j > p->key_lens[b] - p->n_q + i", "j > i"),
+    "window_one_sided": ("(j > i + p->window || j < i - p->window)", "(j > i + p->window)"),
+    "window_off_by_one": ("(j > i + p->window || j < i - p->window)", "(j >= i + p->window || j <= i - p->window)"),
 }
 
 _CHILD = r"""
