@@ -97,12 +97,14 @@ def weak_scaling_tflops(flops_per_rank_step: float, steps: int, max_total_ms: fl
 
 
 def mask_name(mode):
-    return {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding", 4: "decode"}[mode]
+    names = {1: "causal", 2: "key_padding", 4: "decode", 8: "window"}
+    return "+".join(v for k, v in names.items() if mode & k) or "none"
 
 
 def config_of(w, extra=None):
     cfg = {"workload": w.name, "B": w.B, "h": w.H, "n_q": w.n_q, "n_k": w.n_k, "d_k": w.d_k, "d_v": w.d_v,
            "mask": mask_name(w.mask_mode), "inputs": f"N(0,1) x {w.input_scale}, seed {w.seed}",
+           **({"window": w.window} if w.mask_mode & W.MASK_WINDOW else {}),
            "flops": "algorithmic: 2*(d_k+d_v) per legal (query, key) pair"}
     if extra:
         cfg.update(extra)
@@ -171,7 +173,13 @@ def oracle_rows_flops(w, ids, key_lens):
         lim = np.minimum(lim, key_lens[b])
     if w.mask_mode & W.MASK_CAUSAL:
         lim = np.minimum(lim, i + 1)
-    return float(2 * (w.d_k + w.d_v) * lim.sum())
+    lo = np.zeros_like(lim)
+    if w.mask_mode & W.MASK_WINDOW:
+        lim = np.minimum(lim, i + w.window + 1)
+        lo = np.maximum(lo, i - w.window)
+    if w.mask_mode & W.MASK_DECODE:
+        lim = np.minimum(lim, key_lens[b] - w.n_q + i + 1)
+    return float(2 * (w.d_k + w.d_v) * np.maximum(lim - lo, 0).sum())
 
 
 def time_oracle(w, inputs, ids, threads):
@@ -182,7 +190,7 @@ def time_oracle(w, inputs, ids, threads):
     orc = oracle.Oracle()
     q, k, v, kl = inputs
     t0 = time.perf_counter()
-    orc.attention_rows(q, k, v, w.scale, ids, w.mask_mode, kl, n_threads=threads)
+    orc.attention_rows(q, k, v, w.scale, ids, w.mask_mode, kl, n_threads=threads, window=max(w.window, 0))
     return time.perf_counter() - t0
 
 
@@ -235,6 +243,9 @@ def run_ours(args, w):
     def step():
         if decode:
             attn.attn_decode(qd, kd, vd, out, kld, ws, lse, w.scale, stream)
+        elif w.mask_mode & W.MASK_WINDOW:
+            attn.attn_fwd_local(qd, kd, vd, out, w.window, lse, w.scale, w.mask_mode & ~W.MASK_WINDOW, key_lens,
+                                stream)
         else:
             attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens, stream)
 
@@ -349,6 +360,9 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world):
             kld.copy_(klh, non_blocking=True)
         if decode:
             attn.attn_decode(qd, kd, vd, out, kld, ws, None, w.scale, stream)
+        elif w.mask_mode & W.MASK_WINDOW:
+            attn.attn_fwd_local(qd, kd, vd, out, w.window, None, w.scale, w.mask_mode & ~W.MASK_WINDOW,
+                                kld if use_kl else None, stream)
         else:
             attn.attn_fwd(qd, kd, vd, out, None, w.scale, w.mask_mode, kld if use_kl else None, stream)
         outh.copy_(out, non_blocking=True)

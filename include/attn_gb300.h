@@ -79,6 +79,22 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
              int mask_mode, const int32_t* key_lens, void* stream);
 
 /*
+ * attn_fwd_local -- restricted (local-window) self-attention, bf16, on the same
+ * tensor-core kernel as attn_fwd. The pages propose, for very long sequences,
+ * letting each position attend only to positions within a neighbourhood r, which
+ * lowers the cost from O(n^2 d) to O(r n d) (csdn blog section 4.3 and "future
+ * work"; vlmlib.cn "limitations"). Here r = `window` is a radius: key j is legal
+ * for query i only if |i - j| <= window, in addition to whatever mask_mode imposes
+ * (ATTN_MASK_CAUSAL makes the window one-sided, i - window <= j <= i;
+ * ATTN_MASK_KEY_PADDING as in attn_fwd). Self-attention only: q, k, v, out are
+ * [B, h, n, d]. K/V tiles outside every row's window are never loaded.
+ * window >= 0 (ATTN_ERR_INVALID otherwise); other rules as attn_fwd.
+ */
+int attn_fwd_local(const void* q, const void* k, const void* v, void* out, float* lse,
+                   int B, int h, int n, int d_k, int d_v, float scale, int window,
+                   int mask_mode, const int32_t* key_lens, void* stream);
+
+/*
  * attn_fwd_f32 -- float32 inputs and output, float32 arithmetic throughout
  * (CUDA cores). Same semantics and conventions as attn_fwd; pointers 4-byte
  * aligned; 1 <= d_k, d_v <= 256, otherwise ATTN_ERR_UNSUPPORTED.

@@ -63,3 +63,11 @@ def test_decode_legal_pairs_and_bytes():
     for n_q in (1, 3, 5):
         want = int(oracle.legal_mask(3, n_q, 9, oracle.MASK_DECODE, kl2).sum())
         assert W.legal_pairs(3, 1, n_q, 9, W.MASK_DECODE, kl2) == want
+
+
+def test_window_legal_pairs():
+    kl = np.array([9, 5], np.int32)
+    for mode in (W.MASK_WINDOW, W.MASK_WINDOW | W.MASK_CAUSAL, W.MASK_WINDOW | W.MASK_KEY_PADDING):
+        for r in (0, 2, 20):
+            want = int(oracle.legal_mask(2, 9, 9, mode, kl, window=r).sum()) * 3
+            assert W.legal_pairs_window(2, 3, 9, mode, r, kl) == want

@@ -38,6 +38,8 @@ def lib() -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
         L.attn_fwd.restype = i
+        L.attn_fwd_local.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
+        L.attn_fwd_local.restype = i
         L.attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
         L.attn_fwd_f32.restype = i
         L.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
@@ -100,6 +102,28 @@ def _call(fn, q, k, v, out, lse, scale, mask_mode, key_lens, stream, dtype, wher
 def attn_fwd(q, k, v, out, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
     """bf16 forward into caller-provided ``out`` (and optional fp32 ``lse``)."""
     return _call(lib().attn_fwd, q, k, v, out, lse, scale, mask_mode, key_lens, stream, torch.bfloat16, "attn_fwd")
+
+
+def attn_fwd_local(q, k, v, out, window, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
+    """Local-window (restricted) self-attention, bf16: key j is legal for query i only
+    if |i - j| <= window (plus mask_mode)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check(t, n, torch.bfloat16)
+    B, H, n, d_k = q.shape
+    d_v = v.shape[3]
+    if k.shape != (B, H, n, d_k) or v.shape != (B, H, n, d_v) or out.shape != (B, H, n, d_v):
+        raise ValueError("local attention is self-attention: q, k, v, out must share B, H, n")
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 3)
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, 1)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    st = lib().attn_fwd_local(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, n, d_k, d_v, float(scale),
+                              int(window), int(mask_mode), _ptr(key_lens), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_local")
+    return out
 
 
 def attn_fwd_f32(q, k, v, out, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):

@@ -57,7 +57,22 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   attn::PFN_encodeTiled enc = tensor_map_encoder();
   if (!enc) return ATTN_ERR_CUDA;
   attn::TcArgs a{q, k, v, out, lse, B, h, n_q, n_k, d_k, scale, mask_mode, key_lens,
-                 static_cast<cudaStream_t>(stream)};
+                 static_cast<cudaStream_t>(stream), -1};
+  return attn::launch_attn_tc(a, enc);
+}
+
+int attn_fwd_local(const void* q, const void* k, const void* v, void* out, float* lse, int B, int h, int n,
+                   int d_k, int d_v, float scale, int window, int mask_mode, const int32_t* key_lens,
+                   void* stream) {
+  int st = check_common(q, k, v, out, lse, B, h, n, n, d_k, d_v, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (window < 0) return ATTN_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::TcArgs a{q, k, v, out, lse, B, h, n, n, d_k, scale, mask_mode, key_lens,
+                 static_cast<cudaStream_t>(stream), window};
   return attn::launch_attn_tc(a, enc);
 }
 

@@ -115,6 +115,7 @@ struct Params {
   float* lse;
   const int32_t* key_lens;
   int H, n_q, n_k, mask_mode;
+  int window;  // local-window radius, or -1 for none
   int BH, num_qblocks;
   float scale_log2;  // scale * log2(e)
 };
@@ -144,13 +145,32 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) return;
 }
 
-// Number of K/V tiles Q tile t (rows [r0, r0+128)) must visit.
+// Number of K/V tiles (from tile 0) the Q tile of rows [r0, r0+128) must visit.
 __device__ __forceinline__ int tiles_for(int r0, int n_q, int kv_tiles, bool causal) {
   if (r0 >= n_q) return 0;
   return causal ? min(kv_tiles, r0 / BN + 1) : kv_tiles;
 }
 
-template <int D>
+// K/V tiles [jb, jb + n) that the Q tile of rows [r0, r0+128) must visit: the
+// tiles holding a key that is legal for at least one of its rows.
+__device__ __forceinline__ void tile_range(int r0, int n_q, int kv_len, bool causal, int window, int& jb, int& n) {
+  jb = 0;
+  n = 0;
+  if (r0 >= n_q) return;
+  int lo = 0, hi = kv_len;
+  if (causal) hi = min(hi, r0 + BM);
+  if (window >= 0) {
+    lo = max(0, r0 - window);
+    hi = min(hi, r0 + BM + window);
+  }
+  if (hi <= lo) return;
+  jb = lo / BN;
+  n = (hi + BN - 1) / BN - jb;
+}
+
+// LOCAL: local-window instantiation (attn_fwd_local). The plain instantiation sees a
+// constant window of -1, so its tile ranges start at tile 0 and fold to constants.
+template <int D, bool LOCAL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -174,10 +194,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const bool causal = (p.mask_mode & 1) != 0;
   int kv_len = p.n_k;
   if (p.mask_mode & 2) kv_len = min(max(p.key_lens[b], 0), p.n_k);
-  const int kv_tiles = (kv_len + BN - 1) / BN;
-  const int n_t0 = tiles_for(row0, p.n_q, kv_tiles, causal);
-  const int n_t1 = tiles_for(row0 + BM, p.n_q, kv_tiles, causal);
-  const int n_max = max(n_t0, n_t1);
+  const int window = LOCAL ? p.window : -1;
+  int jb0 = 0, n_t0, jb1 = 0, n_t1;
+  if constexpr (LOCAL) {
+    tile_range(row0, p.n_q, kv_len, causal, window, jb0, n_t0);
+    tile_range(row0 + BM, p.n_q, kv_len, causal, window, jb1, n_t1);
+  } else {
+    const int kv_tiles = (kv_len + BN - 1) / BN;
+    n_t0 = tiles_for(row0, p.n_q, kv_tiles, causal);
+    n_t1 = tiles_for(row0 + BM, p.n_q, kv_tiles, causal);
+  }
+  // the K/V ring carries tiles J0 .. J0 + n_max - 1 (ring use u holds tile J0 + u);
+  // tile 1 starts no earlier than tile 0, and tile 0 has work whenever tile 1 has
+  const int J0 = jb0;
+  const int n_max = max(jb0 + n_t0, jb1 + n_t1) - J0;
+  const int off1 = jb1 - J0;  // ring use of tile 1's first K/V tile
 
   // ---- set-up: barriers, TMEM
   if (threadIdx.x == 0) {
@@ -234,8 +265,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c)
-          ptx::tma_load_3d(s_k + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + s), c * 64, j * BN,
-                           bh, pol_kv);
+          ptx::tma_load_3d(s_k + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + s), c * 64,
+                           (J0 + j) * BN, bh, pol_kv);
         ok = wait_bar(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER);
         if (!ok) {
           issued = 2 * j + 1;
@@ -243,8 +274,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
         ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c)
-          ptx::tma_load_3d(s_v + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bar(C::B_VFULL + s), c * 64, j * BN,
-                           bh, pol_kv);
+          ptx::tma_load_3d(s_v + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bar(C::B_VFULL + s), c * 64,
+                           (J0 + j) * BN, bh, pol_kv);
         issued = 2 * j + 2;
       }
       if (!ok) {
@@ -265,21 +296,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int t = role & 1;  // Q tile
     const int n_t = t ? n_t1 : n_t0;
     const int n_o = t ? n_t0 : n_t1;  // tiles of the other Q tile
-    // a K/V stage the other Q tile never reads is released twice by this issuer
-    auto release = [&](int b0, int j) {
-      ptx::mma_commit(bar(b0 + j % C::STAGES));
-      if (j >= n_o) ptx::mma_commit(bar(b0 + j % C::STAGES));
+    const int off_t = t ? off1 : 0, off_o = t ? 0 : off1;  // ring use of each tile's first K/V tile
+    // a K/V stage (ring use u) the other Q tile never reads is released twice by this issuer
+    auto release = [&](int b0, int u) {
+      ptx::mma_commit(bar(b0 + u % C::STAGES));
+      if constexpr (LOCAL) {
+        if (u < off_o || u >= off_o + n_o) ptx::mma_commit(bar(b0 + u % C::STAGES));
+      } else {
+        if (u >= n_o) ptx::mma_commit(bar(b0 + u % C::STAGES));
+      }
     };
     if (C::SEP_P && role < 2 && lane == 0 && n_t > 0) {
       // S_t(j) = Q_t K_j^T, as soon as K_j has landed and the softmax has loaded S_t(j-1)
       const uint32_t q_tile = s_q + t * C::TILE_BYTES;
       bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
       for (int j = 0; j < n_t && ok; ++j) {
-        ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA) &&
+        const int u = off_t + j;
+        ok = wait_bar(bar(C::B_KFULL + u % C::STAGES), (u / C::STAGES) & 1, abort_flag, FAULT_MMA) &&
              (j == 0 || wait_bar(bar(C::B_SFREE + t), (j - 1) & 1, abort_flag, FAULT_MMA));
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t k_stage = s_k + (j % C::STAGES) * C::TILE_BYTES;
+        const uint32_t k_stage = s_k + (u % C::STAGES) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
@@ -287,7 +324,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                       ptx::sdesc_sw128(k_stage + koff, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(bar(C::B_SFULL + t));
-        release(C::B_KEMPTY, j);
+        release(C::B_KEMPTY, u);
       }
       if (!ok) {
         // let every MMA already issued finish before TMEM is released
@@ -301,24 +338,25 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const uint32_t d_o = tmem + C::TMEM_O + t * D;
       bool ok = true;
       for (int j = 0; j < n_t && ok; ++j) {
+        const int u = off_t + j;
         ok = wait_bar(bar(C::B_PFULL + t), j & 1, abort_flag, FAULT_MMA) &&
-             wait_bar(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA);
+             wait_bar(bar(C::B_VFULL + u % C::STAGES), (u / C::STAGES) & 1, abort_flag, FAULT_MMA);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t v_stage = s_v + (j % C::STAGES) * C::TILE_BYTES;
+        const uint32_t v_stage = s_v + (u % C::STAGES) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys = 16 rows of V = two 8-row swizzle groups
           ptx::mma_ts(d_o, a_p + kk * 8, ptx::sdesc_sw128(v_stage + kk * 2048, C::CHUNK_BYTES, 1024), C::IDESC_PV,
                       (j > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(C::B_ODONE + t));
-        release(C::B_VEMPTY, j);
+        release(C::B_VEMPTY, u);
       }
       if (!ok) {
         ptx::mma_commit(bar(C::B_DRAIN + role));
         drain_wait(bar(C::B_DRAIN + role), 0);
       }
     }
-    if (!C::SEP_P && role == 0 && lane == 0 && n_max > 0) {
+    if (!C::SEP_P && !LOCAL && role == 0 && lane == 0 && n_max > 0) {
       // P_t lives in S_t, so S_t(j) must follow PV_t(j-1). One issuer runs, in order,
       //   PV0(j-1), S0(j), PV1(j-1), S1(j)
       // keeping each tile's hand-off short while the other tile's softmax runs.
@@ -374,6 +412,61 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         drain_wait(bar(C::B_DRAIN), 0);
       }
     }
+    if (!C::SEP_P && LOCAL && role == 0 && lane == 0 && n_max > 0) {
+      // the same issuer for the local-window instantiation, whose two Q tiles start at
+      // different K/V tiles
+      // Q tile tt uses ring uses [lo_tt[tt], hi_tt[tt]); j below is the ring use
+      const int lo_tt[2] = {0, off1};
+      const int hi_tt[2] = {n_t0, off1 + n_t1};
+      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
+      ptx::tc_fence_after();
+      for (int j = 0; j <= n_max && ok; ++j) {
+        if (j < n_max) {
+          ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          if (!ok) break;
+        }
+        if (j >= 1) {
+          ok = wait_bar(bar(C::B_VFULL + (j - 1) % C::STAGES), ((j - 1) / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          if (!ok) break;
+        }
+        ptx::tc_fence_after();
+        for (int tt = 0; tt < 2; ++tt) {
+          if (j > lo_tt[tt] && j <= hi_tt[tt]) {
+            ok = wait_bar(bar(C::B_PFULL + tt), (j - 1 - lo_tt[tt]) & 1, abort_flag, FAULT_MMA);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t v_stage = s_v + ((j - 1) % C::STAGES) * C::TILE_BYTES;
+            const uint32_t d_o = tmem + C::TMEM_O + tt * D;
+            const uint32_t a_p = tmem + tt * BN;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t bdesc = ptx::sdesc_sw128(v_stage + kk * 2048, C::CHUNK_BYTES, 1024);
+              ptx::mma_ts(d_o, a_p + kk * 8, bdesc, C::IDESC_PV, (j - lo_tt[tt] > 1 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(bar(C::B_ODONE + tt));
+          }
+          if (j >= lo_tt[tt] && j < hi_tt[tt]) {
+            const uint32_t q_tile = s_q + tt * C::TILE_BYTES;
+            const uint32_t k_stage = s_k + (j % C::STAGES) * C::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+              const uint64_t adesc = ptx::sdesc_sw128(q_tile + koff, 16, 1024);
+              const uint64_t bdesc = ptx::sdesc_sw128(k_stage + koff, 16, 1024);
+              ptx::mma_ss(tmem + tt * BN, adesc, bdesc, C::IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(bar(C::B_SFULL + tt));
+          }
+        }
+        if (!ok) break;
+        if (j < n_max) ptx::mma_commit(bar(C::B_KEMPTY + j % C::STAGES));
+        if (j >= 1) ptx::mma_commit(bar(C::B_VEMPTY + (j - 1) % C::STAGES));
+      }
+      if (!ok) {
+        ptx::mma_commit(bar(C::B_DRAIN));
+        drain_wait(bar(C::B_DRAIN), 0);
+      }
+    }
     __syncwarp();
     }
   } else {
@@ -383,6 +476,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int r = (warp & 3) * 32 + lane;     // row within the tile = TMEM lane
     const int i = row0 + t * BM + r;          // query row
     const int n_tiles = t ? n_t1 : n_t0;
+    const int jb = t ? jb1 : jb0;             // first K/V tile of this Q tile
+    constexpr bool windowed = LOCAL;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_off + t * BN;
     const uint32_t t_p = tmem + lane_off + C::TMEM_P + t * C::TMEM_P_STRIDE;
@@ -401,17 +496,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       for (int q4 = 0; q4 < 4; ++q4) ptx::tmem_ld32(t_s + q4 * 32, sr[q4]);
       ptx::tmem_wait_ld();
 
-      // mask: key-length boundary and the causal diagonal
-      const int j0 = j * BN;
-      const bool edge = (j0 + BN > kv_len) || (causal && j0 + BN - 1 > row0 + t * BM);
+      // mask: key-length boundary, the causal diagonal, the local window
+      const int j0 = (jb + j) * BN;
+      const bool edge = (j0 + BN > kv_len) || (causal && j0 + BN - 1 > row0 + t * BM) || windowed;
       if (edge) {
-        int lim = kv_len - j0;
+        int lim = kv_len - j0;  // columns [first, lim) are legal
         if (causal) lim = min(lim, i - j0 + 1);
+        int first = 0;
+        if (windowed) {
+          lim = min(lim, i + window + 1 - j0);
+          first = i - window - j0;
+        }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
           for (int x = 0; x < 32; ++x)
-            if (q4 * 32 + x >= lim) sr[q4][x] = __float_as_uint(-INFINITY);
+            if (q4 * 32 + x >= lim || q4 * 32 + x < first) sr[q4][x] = __float_as_uint(-INFINITY);
       }
       // row maximum: eight independent 3-input max chains over 16 columns each
       auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
@@ -540,21 +640,16 @@ CUresult encode_map(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D>
-int launch(const TcArgs& a, PFN_encodeTiled enc) {
+template <int D, bool LOCAL>
+int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv) {
   using C = Cfg<D>;
   // the shared-memory opt-in is per device; set it once for each device used
   static std::atomic<bool> attr_done[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  CUtensorMap mq, mk, mv;
-  if (encode_map(enc, &mq, a.q, D, a.n_q, a.B * a.H) != CUDA_SUCCESS ||
-      encode_map(enc, &mk, a.k, D, a.n_k, a.B * a.H) != CUDA_SUCCESS ||
-      encode_map(enc, &mv, a.v, D, a.n_k, a.B * a.H) != CUDA_SUCCESS)
-    return ATTN_ERR_UNSUPPORTED;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_done[dev].store(true, std::memory_order_release);
   }
@@ -566,13 +661,24 @@ int launch(const TcArgs& a, PFN_encodeTiled enc) {
   p.n_q = a.n_q;
   p.n_k = a.n_k;
   p.mask_mode = a.mask_mode;
+  p.window = a.window;
   p.BH = a.B * a.H;
   p.num_qblocks = (a.n_q + 2 * BM - 1) / (2 * BM);
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   const long long grid = (long long)p.BH * p.num_qblocks;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_fwd_tc_kernel<D><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, LOCAL><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D>
+int launch(const TcArgs& a, PFN_encodeTiled enc) {
+  CUtensorMap mq, mk, mv;
+  if (encode_map(enc, &mq, a.q, D, a.n_q, a.B * a.H) != CUDA_SUCCESS ||
+      encode_map(enc, &mk, a.k, D, a.n_k, a.B * a.H) != CUDA_SUCCESS ||
+      encode_map(enc, &mv, a.v, D, a.n_k, a.B * a.H) != CUDA_SUCCESS)
+    return ATTN_ERR_UNSUPPORTED;
+  return a.window >= 0 ? launch_variant<D, true>(a, mq, mk, mv) : launch_variant<D, false>(a, mq, mk, mv);
 }
 
 }  // namespace

@@ -27,6 +27,7 @@ struct TcArgs {
   int mask_mode;
   const int32_t* key_lens;
   cudaStream_t stream;
+  int window;  // local-window radius (>= 0), or -1 for none
 };
 
 // Validated arguments of one fp32 call.

@@ -23,7 +23,7 @@ import math
 
 import numpy as np
 
-MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_DECODE = 0, 1, 2, 4
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_DECODE, MASK_WINDOW = 0, 1, 2, 4, 8
 SEED_BASE = 20170612
 
 
@@ -41,6 +41,7 @@ class Workload:
     key_len_range: tuple | None = None
     input_scale: float = 1.0
     index: int = 0
+    window: int = -1  # local-window radius (MASK_WINDOW), -1 for none
 
     @property
     def seed(self) -> int:
@@ -53,6 +54,8 @@ class Workload:
 
     def legal_pairs(self, key_lens=None) -> int:
         """Number of legal (query, key) pairs over all heads."""
+        if self.mask_mode & MASK_WINDOW:
+            return legal_pairs_window(self.B, self.H, self.n_q, self.mask_mode, self.window, key_lens)
         return legal_pairs(self.B, self.H, self.n_q, self.n_k, self.mask_mode, key_lens)
 
     def algorithmic_flops(self, key_lens=None) -> float:
@@ -90,6 +93,8 @@ def legal_pairs(B, H, n_q, n_k, mask_mode, key_lens=None) -> int:
             L = min(int(key_lens[b]), n_k)
             total += sum(max(0, L - n_q + i + 1) for i in range(n_q))
             continue
+        if mask_mode & MASK_WINDOW:
+            raise ValueError("use legal_pairs_window for local-window workloads")
         if mask_mode & MASK_CAUSAL:
             # query i sees keys 0..min(i, lim-1)
             full = min(n_q, lim)  # rows whose causal limit i+1 <= lim
@@ -99,8 +104,20 @@ def legal_pairs(B, H, n_q, n_k, mask_mode, key_lens=None) -> int:
     return total * H
 
 
-def _wl(index, name, B, H, n_q, n_k, d, dtype, mask, lens=None, scale=1.0):
-    return Workload(name, B, H, n_q, n_k, d, d, dtype, mask, lens, scale, index)
+def legal_pairs_window(B, H, n, mask_mode, window, key_lens=None) -> int:
+    """Legal pairs of local-window self-attention (query i sees |i - j| <= window)."""
+    total = 0
+    for b in range(B):
+        lim = min(n, int(key_lens[b])) if mask_mode & MASK_KEY_PADDING else n
+        for i in range(n):
+            lo = max(0, i - window)
+            hi = min(lim, i + 1 if mask_mode & MASK_CAUSAL else i + window + 1)
+            total += max(0, hi - lo)
+    return total * H
+
+
+def _wl(index, name, B, H, n_q, n_k, d, dtype, mask, lens=None, scale=1.0, window=-1):
+    return Workload(name, B, H, n_q, n_k, d, d, dtype, mask, lens, scale, index, window)
 
 
 WORKLOADS = {w.name: w for w in [
@@ -115,6 +132,9 @@ WORKLOADS = {w.name: w for w in [
     # one autoregressive decoding step (one new query) against a key/value cache
     _wl(8, "decode_b32_h8_q1_k2048_d64", 32, 8, 1, 2048, 64, "bf16", MASK_DECODE, (1024, 2048)),
     _wl(9, "decode_b16_h16_q1_k8192_d64", 16, 16, 1, 8192, 64, "bf16", MASK_DECODE, (4096, 8192)),
+    # restricted self-attention: each position attends to a causal neighbourhood of 512
+    _wl(10, "local_causal_b2_h16_n8192_d64_w511", 2, 16, 8192, 8192, 64, "bf16", MASK_CAUSAL | MASK_WINDOW, None,
+        0.5, 511),
 ]}
 
 
