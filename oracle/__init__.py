@@ -60,7 +60,9 @@ class Oracle:
         self.lib.oracle_attn.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, vp, vp, i]
         self.lib.oracle_attn_rows.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, lp, vp, vp, vp, i]
         self.lib.oracle_attn_weights.argtypes = [vp, vp, i, i, i, i, i, i, d, i, vp, i, vp]
-        for f in (self.lib.oracle_attn, self.lib.oracle_attn_rows, self.lib.oracle_attn_weights):
+        self.lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, vp, vp, vp, i]
+        for f in (self.lib.oracle_attn, self.lib.oracle_attn_rows, self.lib.oracle_attn_weights,
+                  self.lib.oracle_attn_bwd):
             f.restype = ctypes.c_int
 
     @staticmethod
@@ -133,6 +135,34 @@ class Oracle:
         return w
 
 
+    def attention_bwd(self, q, k, v, dout, scale, mask_mode=MASK_NONE, key_lens=None, window=0, n_threads=None):
+        """Gradients ``(dq, dk, dv)`` of ``sum(dout * O)`` in float64."""
+        (q, k, v, dout), dt = self._inputs4(q, k, v, dout)
+        B, H, n_q, d_k = q.shape
+        n_k, d_v = k.shape[2], v.shape[3]
+        if dout.shape != (B, H, n_q, d_v):
+            raise ValueError("dout must have the output's shape")
+        kl = self._lens(mask_mode, key_lens, B)
+        dq = np.empty((B, H, n_q, d_k), np.float64)
+        dk = np.empty((B, H, n_k, d_k), np.float64)
+        dv = np.empty((B, H, n_k, d_v), np.float64)
+        rc = self.lib.oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, dt, B, H, n_q,
+                                      n_k, d_k, d_v, float(scale), int(mask_mode),
+                                      kl.ctypes.data if kl is not None else None, int(window), dq.ctypes.data,
+                                      dk.ctypes.data, dv.ctypes.data, self._threads(n_threads))
+        if rc != 0:
+            raise ValueError("oracle_attn_bwd rejected its arguments")
+        return dq, dk, dv
+
+    @staticmethod
+    def _inputs4(q, k, v, dout):
+        (q, k, v), dt = Oracle._inputs(q, k, v)
+        dout = np.ascontiguousarray(dout)
+        if dout.dtype != q.dtype or dout.ndim != 4:
+            raise TypeError("dout must be 4-D with the inputs' dtype")
+        return (q, k, v, dout), dt
+
+
 def legal_mask(B, n_q, n_k, mask_mode, key_lens=None, window=0) -> np.ndarray:
     """Boolean [B,1,n_q,n_k]: True where key j is a legal connection for query i."""
     i = np.arange(n_q)[:, None]
@@ -168,3 +198,15 @@ def attention_matrix_form(q, k, v, scale, mask_mode=MASK_NONE, key_lens=None, wi
     A = np.where(empty[..., None], 0.0, softmax(S_safe, axis=-1))
     lse = np.where(empty, -np.inf, logsumexp(S_safe, axis=-1))
     return A @ v, lse, A
+
+
+def attention_bwd_matrix_form(q, k, v, dout, scale, mask_mode=MASK_NONE, key_lens=None, window=0):
+    """Matrix form of the gradients of sum(dout * O), float64:
+    dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(P * dP)), dQ = scale dS K,
+    dK = scale dS^T Q, with P from ``attention_matrix_form``."""
+    _, _, P = attention_matrix_form(q, k, v, scale, mask_mode, key_lens, window)
+    q, k, v, dout = widen(q), widen(k), widen(v), widen(dout)
+    dV = np.swapaxes(P, -1, -2) @ dout
+    dP = dout @ np.swapaxes(v, -1, -2)
+    dS = P * (dP - np.sum(P * dP, axis=-1, keepdims=True))
+    return scale * (dS @ k), scale * (np.swapaxes(dS, -1, -2) @ q), dV

@@ -215,3 +215,87 @@ int oracle_attn_weights(const void* q, const void* k, int dtype, int B, int H, i
     }
   return 0;
 }
+
+/* ---------------------------------------------------------------- gradients */
+typedef struct {
+  const problem* p;
+  const void* dout;
+  double *dq, *dk, *dv;
+  int tid, n_threads;
+  int failed;
+} bwd_job;
+
+/* Gradients of one head bh, row by row (definitions in attn_oracle.h). */
+static void bwd_head(const problem* p, const void* dout, int bh, double* w, double* dp, double* dq, double* dk,
+                     double* dv) {
+  const long long qoff = (long long)bh * p->n_q * p->d_k, koff = (long long)bh * p->n_k * p->d_k;
+  const long long voff = (long long)bh * p->n_k * p->d_v, ooff = (long long)bh * p->n_q * p->d_v;
+  for (int i = 0; i < p->n_q; ++i) {
+    double m = row_scores(p, bh, i, w);
+    row_softmax(p->n_k, m, w); /* w_j = P_ij */
+    double sum_pdp = 0.0;
+    for (int j = 0; j < p->n_k; ++j) {
+      double acc = 0.0;
+      for (int t = 0; t < p->d_v; ++t)
+        acc += elem(dout, p->dtype, ooff + (long long)i * p->d_v + t) * elem(p->v, p->dtype, voff + (long long)j * p->d_v + t);
+      dp[j] = acc;
+      sum_pdp += w[j] * acc;
+    }
+    for (int j = 0; j < p->n_k; ++j) {
+      const double ds = w[j] * (dp[j] - sum_pdp);
+      for (int t = 0; t < p->d_k; ++t) {
+        dq[qoff + (long long)i * p->d_k + t] += p->scale * ds * elem(p->k, p->dtype, koff + (long long)j * p->d_k + t);
+        dk[koff + (long long)j * p->d_k + t] += p->scale * ds * elem(p->q, p->dtype, qoff + (long long)i * p->d_k + t);
+      }
+      for (int t = 0; t < p->d_v; ++t)
+        dv[voff + (long long)j * p->d_v + t] += w[j] * elem(dout, p->dtype, ooff + (long long)i * p->d_v + t);
+    }
+  }
+}
+
+static void* bwd_worker(void* arg) {
+  bwd_job* jb = (bwd_job*)arg;
+  const problem* p = jb->p;
+  double* w = (double*)malloc(sizeof(double) * (size_t)p->n_k);
+  double* dp = (double*)malloc(sizeof(double) * (size_t)p->n_k);
+  if (!w || !dp) {
+    jb->failed = 1;
+  } else {
+    for (int bh = jb->tid; bh < p->B * p->H; bh += jb->n_threads) bwd_head(p, jb->dout, bh, w, dp, jb->dq, jb->dk, jb->dv);
+  }
+  free(w);
+  free(dp);
+  return NULL;
+}
+
+int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype, int B, int H, int n_q,
+                    int n_k, int d_k, int d_v, double scale, int mask_mode, const int* key_lens, int window, double* dq,
+                    double* dk, double* dv, int n_threads) {
+  problem p = {q, k, v, dtype, B, H, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens, window};
+  if (check(&p) != 0 || !v || !dout || !dq || !dk || !dv) return -1;
+  memset(dq, 0, sizeof(double) * (size_t)B * H * n_q * d_k);
+  memset(dk, 0, sizeof(double) * (size_t)B * H * n_k * d_k);
+  memset(dv, 0, sizeof(double) * (size_t)B * H * n_k * d_v);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > B * H) n_threads = B * H;
+  bwd_job* jobs = (bwd_job*)calloc((size_t)n_threads, sizeof(bwd_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
+  if (!jobs || !th) {
+    free(jobs);
+    free(th);
+    return -1;
+  }
+  int started = 0;
+  for (int t = 0; t < n_threads; ++t) {
+    jobs[t] = (bwd_job){&p, dout, dq, dk, dv, t, n_threads, 0};
+    if (pthread_create(&th[t], NULL, bwd_worker, &jobs[t]) != 0) break;
+    ++started;
+  }
+  for (int t = started; t < n_threads; ++t) bwd_worker(&jobs[t]);
+  int rc = 0;
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  for (int t = 0; t < n_threads; ++t) rc |= jobs[t].failed;
+  free(jobs);
+  free(th);
+  return rc ? -1 : 0;
+}

@@ -69,6 +69,19 @@ int oracle_attn_weights(const void* q, const void* k, int dtype,
                         int B, int H, int n_q, int n_k, int d_k, double scale,
                         int mask_mode, const int* key_lens, int window, double* weights);
 
+/* Gradients of L = sum(dout * O) with respect to Q, K and V (training needs them:
+ * attention-paper-guide section 05, vlmlib.cn "training"), for the same mask
+ * semantics. dout has O's shape and the inputs' dtype. Per row i:
+ *   P_i  = softmax row of the forward (illegal entries exactly 0)
+ *   dP_ij = dout_i . v_j
+ *   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)       (the softmax Jacobian)
+ *   dq_i  = scale sum_j dS_ij k_j,  dk_j += scale dS_ij q_i,  dv_j += P_ij dout_i
+ * dq: B*H*n_q*d_k, dk: B*H*n_k*d_k, dv: B*H*n_k*d_v doubles. Threads split the heads. */
+int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                    int B, int H, int n_q, int n_k, int d_k, int d_v, double scale,
+                    int mask_mode, const int* key_lens, int window,
+                    double* dq, double* dk, double* dv, int n_threads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -371,4 +371,77 @@ def pin_window_matrix_form(orc):
         assert np.abs(orc.attention_weights(q, k, 0.3, mode, kl, window=r) - A).max() < 1e-12
 
 
+# ---------------------------------------------------------------- gradients (training)
+def _loss(orc, q, k, v, dout, scale, mode, kl, window=0):
+    out, _ = orc.attention(q, k, v, scale, mode, kl, window=window)
+    return float(np.sum(out * dout))
+
+
+def pin_bwd_finite_differences(orc):
+    """The gradients of L = sum(dout * O) match central finite differences of the
+    (pinned) forward oracle, element by element, for every mask and a cross shape."""
+    rng = np.random.Generator(np.random.PCG64(50))
+    cases = [(4, 5, 0), (4, 5, P), (5, 5, C), (5, 5, C | P), (5, 5, WIN | C)]
+    for n_q, n_k, mode in cases:
+        q = rng.standard_normal((1, 2, n_q, 3))
+        k = rng.standard_normal((1, 2, n_k, 3))
+        v = rng.standard_normal((1, 2, n_k, 2))
+        dout = rng.standard_normal((1, 2, n_q, 2))
+        kl = np.array([3], np.int32)
+        win = 1
+        dq, dk, dv = orc.attention_bwd(q, k, v, dout, 0.7, mode, kl, window=win)
+        h = 1e-6
+        for x, g in ((q, dq), (k, dk), (v, dv)):
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = _loss(orc, q, k, v, dout, 0.7, mode, kl, win)
+                x[idx] = old - h
+                lm = _loss(orc, q, k, v, dout, 0.7, mode, kl, win)
+                x[idx] = old
+                assert abs((lp - lm) / (2 * h) - g[idx]) < 1e-7, (mode, idx)
+
+
+def pin_bwd_torch_autograd(orc):
+    """Library cross-check: torch float64 autograd of softmax(scale QK^T + mask) V."""
+    import torch
+
+    q, k, v = _rand(51, 2, 2, 6, 6, 4, 3)
+    dout = np.random.Generator(np.random.PCG64(52)).standard_normal((2, 2, 6, 3))
+    kl = np.array([6, 4], np.int32)
+    for mode in (0, C, P, C | P):
+        mask = torch.from_numpy(np.where(oracle.legal_mask(2, 6, 6, mode, kl), 0.0, -np.inf))
+        tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+        out = torch.softmax(0.45 * tq @ tk.transpose(-1, -2) + mask, dim=-1) @ tv
+        (out * torch.from_numpy(dout)).sum().backward()
+        dq, dk, dv = orc.attention_bwd(q, k, v, dout, 0.45, mode, kl)
+        for a, b in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            assert np.abs(a - b.numpy()).max() < 1e-12
+
+
+def pin_bwd_matrix_form(orc):
+    q, k, v = _rand(53, 2, 3, 7, 9, 4, 5)
+    dout = np.random.Generator(np.random.PCG64(54)).standard_normal((2, 3, 7, 5))
+    kl = np.array([9, 5], np.int32)
+    for mode in (0, P):
+        g1 = orc.attention_bwd(q, k, v, dout, 0.3, mode, kl)
+        g2 = oracle.attention_bwd_matrix_form(q, k, v, dout, 0.3, mode, kl)
+        for a, b in zip(g1, g2):
+            assert np.abs(a - b).max() < 1e-12
+
+
+def pin_bwd_shift_invariance_and_dead_keys(orc):
+    """Rows of dS sum to zero, so dQ, dK and dV do not change when every key moves by a
+    common u (rockcohen.cc section 3.2, score differences only); keys that no query may
+    see (padding) get exactly zero dK and dV."""
+    q, k, v = _rand(55, 2, 1, 5, 6, 3, 2)
+    dout = np.random.Generator(np.random.PCG64(56)).standard_normal((2, 1, 5, 2))
+    kl = np.array([6, 4], np.int32)
+    g = orc.attention_bwd(q, k, v, dout, 0.6, P, kl)
+    g2 = orc.attention_bwd(q, k + np.array([0.5, -1.0, 2.0]), v, dout, 0.6, P, kl)
+    for a, b in zip(g, g2):
+        assert np.abs(a - b).max() < 1e-12
+    assert np.all(g[1][1, :, 4:] == 0.0) and np.all(g[2][1, :, 4:] == 0.0)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -37,6 +37,12 @@ MUTANTS = {
     "decode_off_by_one": ("j > p->key_lens[b] - p->n_q + i", "j >= p->key_lens[b] - p->n_q + i"),
     "decode_start_aligned": ("j > p->key_lens[b] - p->n_q + i", "j > i"),
     "window_one_sided": ("(j > i + p->window || j < i - p->window)", "(j > i + p->window)"),
+    "bwd_no_jacobian_correction": ("const double ds = w[j] * (dp[j] - sum_pdp);", "const double ds = w[j] * dp[j];"),
+    "bwd_jacobian_sign": ("const double ds = w[j] * (dp[j] - sum_pdp);", "const double ds = w[j] * (sum_pdp - dp[j]);"),
+    "bwd_dk_unscaled": ("dk[koff + (long long)j * p->d_k + t] += p->scale * ds *", "dk[koff + (long long)j * p->d_k + t] += ds *"),
+    "bwd_dq_uses_q": ("dq[qoff + (long long)i * p->d_k + t] += p->scale * ds * elem(p->k, p->dtype, koff + (long long)j * p->d_k + t);",
+                      "dq[qoff + (long long)i * p->d_k + t] += p->scale * ds * elem(p->q, p->dtype, qoff + (long long)i * p->d_k + t);"),
+    "bwd_dv_unweighted": ("dv[voff + (long long)j * p->d_v + t] += w[j] *", "dv[voff + (long long)j * p->d_v + t] += (w[j] > 0.0) *"),
     "window_off_by_one": ("(j > i + p->window || j < i - p->window)", "(j >= i + p->window || j <= i - p->window)"),
 }
 
