@@ -18,7 +18,8 @@ import oracle
 
 MUTANTS = {
     "scale_dropped": ("s[j] = p->scale * dot;", "s[j] = dot;"),
-    "k_transposed": ("koff + (long long)j * p->d_k + t", "koff + (long long)t * p->n_k + j"),
+    "k_transposed": ("elem(p->q, p->dtype, qoff + t) * elem(p->k, p->dtype, koff + (long long)j * p->d_k + t)",
+                     "elem(p->q, p->dtype, qoff + t) * elem(p->k, p->dtype, koff + (long long)t * p->n_k + j)"),
     "causal_flipped": ("&& j > i) return 0;", "&& j < i) return 0;"),
     "causal_off_by_one": ("&& j > i) return 0;", "&& j >= i) return 0;"),
     "padding_off_by_one": ("j >= p->key_lens[b]", "j > p->key_lens[b]"),
@@ -27,7 +28,8 @@ MUTANTS = {
     "exp_sign": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
     "not_normalised": ("s[j] = s[j] / l;", "s[j] = s[j];"),
     "lse_missing_log": ("? m + log(l) :", "? m + l :"),
-    "v_row_stride": ("voff + (long long)j * p->d_v + t", "voff + (long long)j * p->d_k + t"),
+    "v_row_stride": ("o[t] += s[j] * elem(p->v, p->dtype, voff + (long long)j * p->d_v + t)",
+                     "o[t] += s[j] * elem(p->v, p->dtype, voff + (long long)j * p->d_k + t)"),
     "k_head_offset": ("long long koff = (long long)bh * p->n_k * p->d_k;",
                       "long long koff = (long long)(bh / p->H) * p->n_k * p->d_k;"),
     "v_head_offset": ("long long voff = (long long)bh * p->n_k * p->d_v;",
