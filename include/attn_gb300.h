@@ -165,13 +165,47 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* cache_lens, void* stream);
 
 /*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs (one fp32 per
+ * query row: D_i below). Returns 0 for an invalid shape.
+ */
+size_t attn_bwd_workspace_size(int B, int h, int n_q);
+
+/*
+ * attn_bwd -- gradients of attn_fwd with respect to q, k and v, given the gradient
+ * dout of the output. Training the model by gradient descent needs them
+ * (attention-paper-guide section 05; vlmlib.cn "training"). With P the softmax
+ * weights of Eq. (1) (rockcohen.cc section 5.1) recomputed from lse,
+ * P[i,j] = exp(scale * q_i . k_j - lse_i) on legal pairs and 0 on illegal ones:
+ *   dv_j = sum_i P[i,j] dout_i
+ *   dP[i,j] = dout_i . v_j,  D_i = dout_i . out_i,  dS[i,j] = P[i,j] (dP[i,j] - D_i)
+ *   dq_i = scale sum_j dS[i,j] k_j,      dk_j = scale sum_i dS[i,j] q_i
+ *   q, k, v, out, dout: bf16 as in attn_fwd (out and lse are those attn_fwd returned
+ *           for the same q, k, v, scale, mask_mode and key_lens; lse is required)
+ *   dq [B, h, n_q, d], dk, dv [B, h, n_k, d]: bf16, written in full (a key that no
+ *           query may see gets dk = dv = 0; a query with no legal key gets dq = 0)
+ *   workspace: device scratch of at least attn_bwd_workspace_size(B, h, n_q) bytes,
+ *           16-byte aligned, owned by the caller, contents undefined on return;
+ *           concurrent calls must not share it.
+ * mask_mode and key_lens as in attn_fwd. Supported: d_k == d_v in {64, 128}.
+ * Numerics: S and dP accumulate in fp32 on the tensor cores; P and dS are rounded to
+ * bf16 before the three products that consume them, which accumulate in fp32; D_i
+ * is accumulated in fp32 from the bf16 out and dout; results are rounded to bf16
+ * once. Three kernels are launched on `stream`, no atomics: the results are
+ * deterministic.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
+             int mask_mode, const int32_t* key_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_fault_status -- synchronises `stream`, then reports whether any kernel of
  * this library on the current device gave up waiting on one of its internal
  * barriers since the last clear (each such wait is bounded in time; a kernel that
  * gives up writes no further output and returns). Returns ATTN_OK,
  * ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA. If `clear` is non-zero the record is reset.
  * `fault_code` (may be NULL) receives the raw record: bit 0 producer, bit 1 MMA
- * issuer, bit 2 softmax, bit 3 epilogue (attn_fwd), bit 4 decode copy (attn_decode).
+ * issuer, bit 2 softmax, bit 3 epilogue (attn_fwd), bit 4 decode copy (attn_decode),
+ * bit 5 gradient kernels (attn_bwd).
  */
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code);
 

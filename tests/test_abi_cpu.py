@@ -116,3 +116,28 @@ def test_decode_workspace_and_argument_checks(L):
     assert call(n_q=17) == attn.ATTN_ERR_UNSUPPORTED
     assert call(d=96) == attn.ATTN_ERR_UNSUPPORTED
     assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID
+
+
+def test_bwd_workspace_and_argument_checks(L):
+    ws = attn.attn_bwd_workspace_size
+    assert ws(2, 3, 500) == 2 * 3 * 500 * 4
+    assert ws(0, 1, 1) == 0 and ws(1, 1, 0) == 0
+    need = ws(2, 3, 500)
+    f = L.attn_bwd
+    ok = dict(q=16, k=32, v=48, out=64, dout=80, lse=96, dq=112, dk=128, dv=144, B=2, h=3, n_q=500, n_k=500,
+              d_k=64, d_v=64, scale=0.125, mask=1, lens=None, ws=160, nbytes=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"], a["h"],
+                 a["n_q"], a["n_k"], a["d_k"], a["d_v"], a["scale"], a["mask"], a["lens"], a["ws"], a["nbytes"],
+                 None)
+    assert call(nbytes=need - 1) == attn.ATTN_ERR_INVALID      # workspace too small
+    for name in ("dout", "lse", "dq", "dk", "dv", "ws"):
+        assert call(**{name: None}) == attn.ATTN_ERR_INVALID
+    assert call(dk=136) == attn.ATTN_ERR_INVALID               # misaligned gradient
+    assert call(n_k=400) == attn.ATTN_ERR_INVALID              # causal needs n_q == n_k
+    assert call(mask=2) == attn.ATTN_ERR_INVALID               # key padding without key_lens
+    assert call(d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(d_v=128) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(scale=float("inf")) == attn.ATTN_ERR_INVALID

@@ -48,6 +48,11 @@ def lib() -> ctypes.CDLL:
         L.attn_decode.restype = i
         L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.attn_decode_noalloc.restype = i
+        L.attn_bwd_workspace_size.argtypes = [i, i, i]
+        L.attn_bwd_workspace_size.restype = ctypes.c_size_t
+        L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, ctypes.c_size_t,
+                               vp]
+        L.attn_bwd.restype = i
         L.attn_fault_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint32)]
         L.attn_fault_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -196,6 +201,42 @@ def attn_decode_noalloc(q, k_cache, v_cache, out, cache_lens, lse=None, scale=No
     if st != ATTN_OK:
         raise AttnError(st, "attn_decode_noalloc")
     return out
+
+
+def attn_bwd_workspace_size(B, H, n_q) -> int:
+    return int(lib().attn_bwd_workspace_size(B, H, n_q))
+
+
+def attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, scale=None, mask_mode=MASK_NONE, key_lens=None,
+             stream=None):
+    """Gradients of attn_fwd into caller-provided ``dq``, ``dk``, ``dv`` (bf16, shaped like
+    q, k, v), given ``dout`` and the forward's ``out`` and fp32 ``lse``; ``workspace`` is a
+    CUDA tensor of at least ``attn_bwd_workspace_size`` bytes."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, torch.bfloat16)
+    B, H, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    if (k.shape != (B, H, n_k, d_k) or v.shape != (B, H, n_k, d_v) or out.shape != (B, H, n_q, d_v)
+            or dout.shape != out.shape or dq.shape != q.shape or dk.shape != k.shape or dv.shape != v.shape):
+        raise ValueError("shape mismatch between q, k, v, out, dout and the gradients")
+    _check(lse, "lse", torch.float32, 3)
+    if lse.shape != (B, H, n_q):
+        raise ValueError("lse must have shape [B, H, n_q]")
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, 1)
+        if key_lens.shape != (B,):
+            raise ValueError("key_lens must have shape [B]")
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, H, n_q, n_k, d_k, d_v, float(scale), int(mask_mode), _ptr(key_lens), _ptr(workspace),
+                        nbytes, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fault_status(stream=None, clear=True):

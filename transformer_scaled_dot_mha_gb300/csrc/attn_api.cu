@@ -125,8 +125,36 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
   return attn::launch_attn_decode_noalloc(a);
 }
 
+size_t attn_bwd_workspace_size(int B, int h, int n_q) {
+  if (B <= 0 || h <= 0 || n_q <= 0 || (long long)B * h > 0x7fffffffLL) return 0;
+  return attn::bwd_workspace_bytes(B, h, n_q);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
+             int mask_mode, const int32_t* key_lens, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_common(q, k, v, out, lse, B, h, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (!dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 16))
+    return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < attn::bwd_workspace_bytes(B, h, n_q)) return ATTN_ERR_INVALID;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::BwdArgs a{q, k, v, out, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, mask_mode, key_lens,
+                  static_cast<cudaStream_t>(stream)};
+  return attn::launch_attn_bwd(a, enc, workspace);
+}
+
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code) {
-  return attn::read_fault_word(static_cast<cudaStream_t>(stream), clear, fault_code);
+  uint32_t w = 0, wb = 0;
+  const int st = attn::read_fault_word(static_cast<cudaStream_t>(stream), clear, &w);
+  if (st == ATTN_ERR_CUDA || attn::read_bwd_fault_word(clear, &wb) != ATTN_OK) return ATTN_ERR_CUDA;
+  w |= wb;
+  if (fault_code) *fault_code = w;
+  return w ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 const char* attn_status_string(int status) {

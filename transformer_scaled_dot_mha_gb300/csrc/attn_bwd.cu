@@ -1,0 +1,510 @@
+// attn_bwd.cu -- gradients of scaled dot-product attention (dQ, dK, dV) on the
+// sm_103a tensor cores, bf16 in and out, fp32 accumulation.
+//
+// For L = sum(dO * O) with O = softmax(scale Q K^T + mask) V (Eq. (1) of "Attention
+// Is All You Need", rockcohen.cc section 5.1; masks of sections 5.3, 6.3), with
+// P the softmax weights recomputed from the forward's log-sum-exp:
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   D_i = sum_j P_ij dP_ij = dO_i . O_i
+//   dQ = scale dS K,   dK = scale dS^T Q
+// (training the model needs them: attention-paper-guide section 05; vlmlib.cn
+// "training").
+//
+// Three kernels, no atomics:
+//   attn_bwd_dot_kernel   D_i = dO_i . O_i (fp32), one warp per row;
+//   attn_bwd_dkdv_kernel  one CTA per 128-key tile of one (b, h); it streams the
+//                         query tiles that can see its keys (Q_i, dO_i by TMA;
+//                         lse_i, D_i by the producer warp), computes
+//                         S^T = K Q_i^T and dP^T = V dO_i^T into TMEM, turns them
+//                         into P^T and dS^T (bf16, written back into TMEM over
+//                         the consumed columns; thread = key = TMEM lane), and
+//                         accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM;
+//   attn_bwd_dq_kernel    one CTA per 128-query tile; it streams the key tiles,
+//                         computes S = Q K_j^T and dP = dO V_j^T, forms dS (thread =
+//                         query) and accumulates dQ += dS K_j.
+// Every operand layout is one the forward kernel already uses: a [rows][d] tile
+// loaded with 128-byte swizzling is a K-major operand along d and an MN-major
+// operand along d. Waits are bounded as in the forward kernel; a wait that runs
+// out records a fault bit (attn_fault_status), every role stops and TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace attn {
+
+__device__ unsigned int g_bwd_fault_word;  // fault record of the gradient kernels
+
+namespace {
+
+constexpr int T = 128;          // rows per tile (queries or keys)
+constexpr int THREADS = 192;    // warps 0-3 elementwise, 4 producer, 5 MMA issuer
+constexpr int WARP_LOAD = 4, WARP_MMA = 5;
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr uint32_t FAULT_BWD = 32;
+
+template <int D>
+struct BCfg {
+  // ring depth; with d = 64 the deeper ring also keeps a second CTA (which would
+  // block on the 512-column TMEM allocation) off the SM
+  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int CHUNK_BYTES = T * 128;
+  static constexpr int TILE_BYTES = T * D * 2;
+  // resident tiles (A operands) and a ring of streamed tile pairs
+  static constexpr int OFF_A0 = 0;                          // K (dkdv) or Q (dq)
+  static constexpr int OFF_A1 = OFF_A0 + TILE_BYTES;        // V (dkdv) or dO (dq)
+  static constexpr int OFF_R0 = OFF_A1 + TILE_BYTES;        // ring: Q_i (dkdv) or K_j (dq)
+  static constexpr int OFF_R1 = OFF_R0 + STAGES * TILE_BYTES;  // ring: dO_i (dkdv) or V_j (dq)
+  static constexpr int OFF_VEC = OFF_R1 + STAGES * TILE_BYTES;  // float lse[STAGES][T], dd[STAGES][T]
+  static constexpr int OFF_BAR = OFF_VEC + 2 * STAGES * T * 4;
+  // barriers: a_full, full[S], empty[S], mm_full, p_full, acc_done, drain
+  static constexpr int B_AFULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_MMFULL = B_EMPTY + STAGES;
+  static constexpr int B_PFULL = B_MMFULL + 1, B_ACC = B_PFULL + 1, B_DRAIN = B_ACC + 1, NUM_BARS = B_DRAIN + 1;
+  static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_ABORT = OFF_SLOT + 4;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+  // TMEM: X [0,128) = S^T or S, Y [128,256) = dP^T or dP, acc0 [256, 256+D), acc1 [256+D, 256+2D)
+  static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
+  static constexpr uint32_t IDESC_NN = ptx::idesc_bf16_f32(T, T, false);  // both operands K-major
+  static constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(T, D, true);  // B MN-major
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct BwdParams {
+  const float* lse;    // [BH][n_q], natural log
+  const float* dd;     // [BH][n_q]  D_i = dO_i . O_i
+  uint16_t* g0;        // dkdv: dK [BH][n_k][D];  dq: dQ [BH][n_q][D]
+  uint16_t* g1;        // dkdv: dV [BH][n_k][D]
+  const int32_t* key_lens;
+  int H, n_q, n_k, mask_mode, BH, tiles;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(&g_bwd_fault_word, FAULT_BWD);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) return;
+}
+
+
+// ------------------------------------------------------------------ D_i = dO_i . O_i
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const uint16_t* out, const uint16_t* dout, float* dd,
+                                                           long long rows) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint32_t* o = reinterpret_cast<const uint32_t*>(out + row * D);
+  const uint32_t* g = reinterpret_cast<const uint32_t*>(dout + row * D);
+  float acc = 0.0f;
+#pragma unroll
+  for (int x = lane; x < D / 2; x += 32) {
+    const uint32_t a = o[x], b = g[x];
+    acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
+    acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) dd[row] = acc;
+}
+
+// Legal key range of query row i of batch b: keys [0, lim).
+__device__ __forceinline__ int key_limit(int i, int kv_len, bool causal) { return causal ? min(kv_len, i + 1) : kv_len; }
+
+// ------------------------------------------------------------------ dK, dV
+// KV tile kt of head bh; query tiles it = q_begin .. tiles-1 (causal: those at or
+// after the key tile). MODE selects the operand roles (see the file comment).
+template <int D, bool DKDV>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                       const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
+                       const BwdParams p) {
+  using C = BCfg<D>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_base = ptx::smem_u32(smem);
+  auto bar = [&](int x) -> uint32_t { return s_base + C::OFF_BAR + 8u * x; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
+  float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // lse[S][T] then dd[S][T]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int bh = blockIdx.x % p.BH;
+  // own tile: keys (DKDV; the low, busiest causal tiles first) or queries (dQ; the
+  // high, busiest causal tiles first)
+  const int own = DKDV ? (int)(blockIdx.x / p.BH) : p.tiles - 1 - (int)(blockIdx.x / p.BH);
+  const int b = bh / p.H;
+  const bool causal = (p.mask_mode & 1) != 0;
+  int kv_len = p.n_k;
+  if (p.mask_mode & 2) kv_len = min(max(p.key_lens[b], 0), p.n_k);
+  const int own0 = own * T;
+  // streamed tiles [s_begin, s_end)
+  int s_begin, s_end;
+  if (DKDV) {  // query tiles that see any key of [own0, own0 + T)
+    s_begin = (causal ? own0 : 0) / T;
+    s_end = (own0 < kv_len) ? (p.n_q + T - 1) / T : s_begin;
+  } else {     // key tiles any query of [own0, own0 + T) sees
+    s_begin = 0;
+    const int hi = causal ? min(kv_len, own0 + T) : kv_len;
+    s_end = (own0 < p.n_q) ? (hi + T - 1) / T : 0;
+  }
+  const int n_s = max(0, s_end - s_begin);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(C::B_AFULL), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar(C::B_FULL + s), DKDV ? 1 + 32 : 1);  // TMA bytes (+ the producer lanes' vector stores)
+      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
+    }
+    ptx::mbar_init(bar(C::B_MMFULL), 1);
+    ptx::mbar_init(bar(C::B_PFULL), T);
+    ptx::mbar_init(bar(C::B_ACC), 1);
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == WARP_LOAD) {
+    // ================================================================ producer (whole warp)
+    bool ok = true;
+    int issued = 0;
+    if (n_s > 0) {
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(C::B_AFULL), 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          ptx::tma_load_3d(s_base + C::OFF_A0 + c * C::CHUNK_BYTES, &tm_a0, bar(C::B_AFULL), c * 64, own0, bh, 0);
+          ptx::tma_load_3d(s_base + C::OFF_A1 + c * C::CHUNK_BYTES, &tm_a1, bar(C::B_AFULL), c * 64, own0, bh, 0);
+        }
+      }
+      for (int u = 0; u < n_s && ok; ++u) {
+        const int st = u % STAGES;
+        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_EMPTY + st), ((u / STAGES) & 1) ^ 1, abort_flag));
+        if (!ok) break;
+        const int r0 = (s_begin + u) * T;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+          for (int c = 0; c < C::CHUNKS; ++c) {
+            ptx::tma_load_3d(s_base + C::OFF_R0 + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_r0, bar(C::B_FULL + st),
+                             c * 64, r0, bh, 0);
+            ptx::tma_load_3d(s_base + C::OFF_R1 + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_r1, bar(C::B_FULL + st),
+                             c * 64, r0, bh, 0);
+          }
+        }
+        if (DKDV) {
+          // lse and D of the 128 queries of this tile (rows past n_q: lse = +inf -> P = 0)
+          for (int x = lane; x < T; x += 32) {
+            const int i = r0 + x;
+            const bool in = i < p.n_q;
+            vec[st * T + x] = in ? p.lse[(size_t)bh * p.n_q + i] : INFINITY;
+            vec[(STAGES + st) * T + x] = in ? p.dd[(size_t)bh * p.n_q + i] : 0.0f;
+          }
+          ptx::mbar_arrive(bar(C::B_FULL + st));
+        }
+        issued = u + 1;
+      }
+    }
+    if (!ok && lane == 0) {
+      drain_wait(bar(C::B_AFULL), 0);
+      for (int u = max(0, issued - STAGES); u < issued; ++u) drain_wait(bar(C::B_FULL + u % STAGES), (u / STAGES) & 1);
+    }
+    __syncwarp();
+  } else if (warp == WARP_MMA) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && n_s > 0) {
+      bool ok = wait_bar(bar(C::B_AFULL), 0, abort_flag);
+      const uint32_t a0 = s_base + C::OFF_A0, a1 = s_base + C::OFF_A1;
+      for (int u = 0; u < n_s && ok; ++u) {
+        const int st = u % STAGES;
+        ok = wait_bar(bar(C::B_FULL + st), (u / STAGES) & 1, abort_flag);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t r0 = s_base + C::OFF_R0 + st * C::TILE_BYTES, r1 = s_base + C::OFF_R1 + st * C::TILE_BYTES;
+        // X = A0 R0^T, Y = A1 R1^T (both operands K-major along d)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          ptx::mma_ss(tmem + C::TM_X, ptx::sdesc_sw128(a0 + koff, 16, 1024), ptx::sdesc_sw128(r0 + koff, 16, 1024),
+                      C::IDESC_NN, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          ptx::mma_ss(tmem + C::TM_Y, ptx::sdesc_sw128(a1 + koff, 16, 1024), ptx::sdesc_sw128(r1 + koff, 16, 1024),
+                      C::IDESC_NN, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_MMFULL));
+        ok = wait_bar(bar(C::B_PFULL), u & 1, abort_flag);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        // DKDV: dV += P^T dO_i (P^T over X), dK += dS^T Q_i (dS^T over Y), B = R1 / R0 MN-major
+        // dQ:   dQ += dS K_j (dS over X), B = R0 MN-major
+#pragma unroll
+        for (int kk = 0; kk < T / 16; ++kk) {
+          if (DKDV) {
+            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::TM_X + kk * 8, ptx::sdesc_sw128(r1 + kk * 2048, C::CHUNK_BYTES, 1024),
+                        C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_Y + kk * 8, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
+                        C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_X + kk * 8, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
+                        C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        ptx::mma_commit(bar(C::B_EMPTY + st));  // the stage's tiles are consumed once these complete
+      }
+      if (ok) ptx::mma_commit(bar(C::B_ACC));
+      if (!ok) {
+        ptx::mma_commit(bar(C::B_DRAIN));
+        drain_wait(bar(C::B_DRAIN), 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ elementwise warpgroup
+    const int r = warp * 32 + lane;  // TMEM lane = own row (key for DKDV, query for dQ)
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int own_row = own0 + r;
+    const float c = p.scale_log2;
+    const float LOG2E = 1.4426950408889634f;
+    // dQ: this thread's query statistics
+    float my_lse2 = 0.0f, my_dd = 0.0f;
+    int my_lim = 0;
+    if (!DKDV && own_row < p.n_q) {
+      my_lse2 = p.lse[(size_t)bh * p.n_q + own_row] * LOG2E;
+      my_dd = p.dd[(size_t)bh * p.n_q + own_row];
+      my_lim = key_limit(own_row, kv_len, causal);
+    }
+    bool ok = true;
+    for (int u = 0; u < n_s && ok; ++u) {
+      const int st = u % STAGES;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_MMFULL), u & 1, abort_flag));
+      // the stage's lse / D vectors (DKDV): already complete, waited on for ordering
+      if (DKDV && ok) ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_FULL + st), (u / STAGES) & 1, abort_flag));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int s0 = (s_begin + u) * T;  // first streamed row (query for DKDV, key for dQ)
+      // four 32-column chunks: load S (X) and dP (Y), write P / dS as bf16 pairs into the
+      // columns already consumed
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t xs[32], ys[32];
+        ptx::tmem_ld32(tmem + lane_off + C::TM_X + ch * 32, xs);
+        ptx::tmem_ld32(tmem + lane_off + C::TM_Y + ch * 32, ys);
+        ptx::tmem_wait_ld();
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          float pp[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = ch * 32 + x + e;
+            bool legal;
+            float lse2, dd;
+            if (DKDV) {  // own key own_row, query s0 + col
+              const int qi = s0 + col;
+              legal = own_row < kv_len && (!causal || qi >= own_row);
+              lse2 = vec[st * T + col] * LOG2E;
+              dd = vec[(STAGES + st) * T + col];
+            } else {     // own query own_row, key s0 + col
+              legal = s0 + col < my_lim;
+              lse2 = my_lse2;
+              dd = my_dd;
+            }
+            const float pv = legal ? ptx::ex2(fmaf(__uint_as_float(xs[x + e]), c, -lse2)) : 0.0f;
+            pp[e] = pv;
+            dsv[e] = pv * (__uint_as_float(ys[x + e]) - dd);
+          }
+          pw[x >> 1] = ptx::pack_bf16x2(pp[0], pp[1]);
+          dw[x >> 1] = ptx::pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // P (dkdv) goes over X, dS over Y (dkdv) or over X (dQ)
+        if (DKDV) {
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                       ::"r"(tmem + lane_off + C::TM_X + ch * 16), "r"(pw[0]), "r"(pw[1]), "r"(pw[2]), "r"(pw[3]), "r"(pw[4]),
+                       "r"(pw[5]), "r"(pw[6]), "r"(pw[7]), "r"(pw[8]), "r"(pw[9]), "r"(pw[10]), "r"(pw[11]), "r"(pw[12]),
+                       "r"(pw[13]), "r"(pw[14]), "r"(pw[15]) : "memory");
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                       ::"r"(tmem + lane_off + C::TM_Y + ch * 16), "r"(dw[0]), "r"(dw[1]), "r"(dw[2]), "r"(dw[3]), "r"(dw[4]),
+                       "r"(dw[5]), "r"(dw[6]), "r"(dw[7]), "r"(dw[8]), "r"(dw[9]), "r"(dw[10]), "r"(dw[11]), "r"(dw[12]),
+                       "r"(dw[13]), "r"(dw[14]), "r"(dw[15]) : "memory");
+        } else {
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                       ::"r"(tmem + lane_off + C::TM_X + ch * 16), "r"(dw[0]), "r"(dw[1]), "r"(dw[2]), "r"(dw[3]), "r"(dw[4]),
+                       "r"(dw[5]), "r"(dw[6]), "r"(dw[7]), "r"(dw[8]), "r"(dw[9]), "r"(dw[10]), "r"(dw[11]), "r"(dw[12]),
+                       "r"(dw[13]), "r"(dw[14]), "r"(dw[15]) : "memory");
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_PFULL));
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    const int n_rows = DKDV ? p.n_k : p.n_q;
+    const bool row_valid = own_row < n_rows;
+    if (ok && n_s > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ACC), 0, abort_flag));
+      if (ok) ptx::tc_fence_after();
+    }
+    if (ok) {
+      // DKDV: g0 = dK = scale * acc0, g1 = dV = acc1; dQ: g0 = dQ = scale * acc0.
+      // A tile with nothing to stream (all keys padding, or rows past the end) writes zeros.
+#pragma unroll
+      for (int which = 0; which < (DKDV ? 2 : 1); ++which) {
+        uint16_t* g = which == 0 ? p.g0 : p.g1;
+        const float mul = which == 0 ? p.scale : 1.0f;
+        const uint32_t col0 = which == 0 ? C::TM_ACC0 : C::TM_ACC1;
+        uint16_t* grow = g + ((size_t)bh * n_rows + (size_t)(row_valid ? own_row : 0)) * D;
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t o[32];
+          if (n_s > 0) {
+            ptx::tmem_ld32(tmem + lane_off + col0 + q4 * 32, o);
+            ptx::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            w[x] = ptx::pack_bf16x2(__uint_as_float(o[2 * x]) * mul, __uint_as_float(o[2 * x + 1]) * mul);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(grow + q4 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+CUresult encode(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int d, int n, int bh) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)n};
+  cuuint32_t box[3] = {64, (cuuint32_t)T, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int D, bool DKDV>
+int set_smem_attr() {
+  static std::atomic<bool> done[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  if (!done[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<D, DKDV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BCfg<D>::SMEM_BYTES) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    done[dev].store(true, std::memory_order_release);
+  }
+  return ATTN_OK;
+}
+
+template <int D>
+int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* dd) {
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv, mdo;
+  if (encode(enc, &mq, a.q, D, a.n_q, BH) != CUDA_SUCCESS || encode(enc, &mk, a.k, D, a.n_k, BH) != CUDA_SUCCESS ||
+      encode(enc, &mv, a.v, D, a.n_k, BH) != CUDA_SUCCESS || encode(enc, &mdo, a.dout, D, a.n_q, BH) != CUDA_SUCCESS)
+    return ATTN_ERR_UNSUPPORTED;
+  if (set_smem_attr<D, true>() != ATTN_OK || set_smem_attr<D, false>() != ATTN_OK) return ATTN_ERR_CUDA;
+  const long long rows = (long long)BH * a.n_q;
+  attn_bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, a.stream>>>(
+      static_cast<const uint16_t*>(a.out), static_cast<const uint16_t*>(a.dout), dd, rows);
+  if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  BwdParams p;
+  p.lse = a.lse;
+  p.dd = dd;
+  p.key_lens = a.key_lens;
+  p.H = a.H;
+  p.n_q = a.n_q;
+  p.n_k = a.n_k;
+  p.mask_mode = a.mask_mode;
+  p.BH = BH;
+  p.scale = a.scale;
+  p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
+  // dK, dV: own = key tiles; A0 = K, A1 = V; streamed R0 = Q, R1 = dO
+  p.g0 = static_cast<uint16_t*>(a.dk);
+  p.g1 = static_cast<uint16_t*>(a.dv);
+  p.tiles = (a.n_k + T - 1) / T;
+  long long grid = (long long)BH * p.tiles;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  attn_bwd_tc_kernel<D, true><<<(unsigned)grid, THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mk, mv, mq, mdo, p);
+  if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  // dQ: own = query tiles; A0 = Q, A1 = dO; streamed R0 = K, R1 = V
+  p.g0 = static_cast<uint16_t*>(a.dq);
+  p.g1 = nullptr;
+  p.tiles = (a.n_q + T - 1) / T;
+  grid = (long long)BH * p.tiles;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  attn_bwd_tc_kernel<D, false><<<(unsigned)grid, THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mq, mdo, mk, mv, p);
+  return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int H, int n_q) { return (size_t)B * H * n_q * sizeof(float); }
+
+int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace) {
+  float* dd = static_cast<float*>(workspace);
+  if (a.d == 64) return launch_bwd<64>(a, enc, dd);
+  if (a.d == 128) return launch_bwd<128>(a, enc, dd);
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+int read_bwd_fault_word(int clear, uint32_t* out) {
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_bwd_fault_word, sizeof w) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (clear) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_bwd_fault_word, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  *out = w;
+  return ATTN_OK;
+}
+
+}  // namespace attn

@@ -57,6 +57,24 @@ struct DecodeArgs {
   cudaStream_t stream;
 };
 
+// Validated arguments of one gradient call (d_k == d_v == d).
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, H, n_q, n_k, d;
+  float scale;
+  int mask_mode;
+  const int32_t* key_lens;
+  cudaStream_t stream;
+};
+
 int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc);   // attn_fwd_tc.cu
 int launch_attn_f32(const F32Args& a);                       // attn_fwd_f32.cu
 int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd_tc.cu
@@ -65,5 +83,8 @@ size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d);  // attn
 int launch_attn_decode(const DecodeArgs& a, void* workspace);            // attn_decode.cu
 int launch_attn_decode_noalloc(const DecodeArgs& a);                     // attn_decode.cu
 int read_decode_fault_word(int clear, uint32_t* out);                   // attn_decode.cu
+size_t bwd_workspace_bytes(int B, int H, int n_q);                       // attn_bwd.cu
+int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_bwd.cu
+int read_bwd_fault_word(int clear, uint32_t* out);                       // attn_bwd.cu
 
 }  // namespace attn
