@@ -8,7 +8,12 @@ tiles in, QK^T, scale, mask, online softmax, PV, normalisation and the bf16 /
 lse stores). FLOPs are algorithmic: 2 (d_k + d_v) per legal query-key pair.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--no-cpu-baseline]
+                  [--impl ours|reference] [--no-cpu-baseline] [--grad]
+
+--grad times the gradients instead (one attn_bwd call per step: D = rowsum(dO*O),
+the dK/dV kernel and the dQ kernel), given the forward's output and lse computed
+once before the timed region; FLOPs are algorithmic, 2 (3 d_k + 2 d_v) per legal
+pair (the five products of the backward pass).
 
 Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
 GPU (independent shards of B*h, no collective on the data path; weak scaling),
@@ -388,6 +393,153 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, attn, flops_step, world):
             "steps": steps, "how": how}
 
 
+# ---------------------------------------------------------------- gradients
+def cpu_baseline_grad(w, inputs, dout):
+    """The oracle's gradients, as they stand, on a bounded sample: whole heads of
+    the workload (one host thread per head)."""
+    import oracle
+
+    if not os.path.exists(oracle.LIB):
+        oracle.build()
+    orc = oracle.Oracle()
+    q, k, v, kl = inputs
+    threads = os.cpu_count() or 1
+    hs = max(1, min(threads, w.H))
+    sl = lambda a: np.ascontiguousarray(a[:1, :hs])
+    kl1 = kl[:1] if w.mask_mode & W.MASK_KEY_PADDING else None
+    t0 = time.perf_counter()
+    orc.attention_bwd(sl(q), sl(k), sl(v), sl(dout), w.scale, w.mask_mode, kl1, n_threads=hs)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * (3 * w.d_k + 2 * w.d_v) * W.legal_pairs(1, hs, w.n_q, w.n_k, w.mask_mode, kl1)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": hs, "kind": "oracle",
+            "sample": f"{hs} whole heads (batch 0) of the workload, fp64 C oracle gradients, {dt:.2f} s wall"}
+
+
+def run_ours_grad(args, w):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from transformer_scaled_dot_mha_gb300 import attn
+
+    attn.lib()
+    seed = shard_seed(w, rank)
+    q, k, v, kl = W.make_inputs(w, seed)
+    dout = W.make_grad_output(w, seed)
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    qd, kd, vd, gd = to_dev(q), to_dev(k), to_dev(v), to_dev(dout)
+    kld = torch.from_numpy(kl).to(dev)
+    key_lens = kld if w.mask_mode & W.MASK_KEY_PADDING else None
+    out = torch.empty((w.B, w.H, w.n_q, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.n_q), dtype=torch.float32, device=dev)
+    attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(attn.attn_bwd_workspace_size(w.B, w.H, w.n_q), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        attn.attn_bwd(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, w.scale, w.mask_mode, key_lens, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} during warm-up")
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop() if rank == 0 else None
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dev)
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} in the timed region")
+    flops_step = w.algorithmic_bwd_flops(kl)
+    ms_per_step = total_ms / args.steps
+    value = weak_scaling_tflops(flops_step, args.steps, total_ms, world)
+
+    # end to end: pinned host Q, K, V, O, dO, lse in; dQ, dK, dV out
+    pin = lambda t: t.cpu().pin_memory()
+    hosts = [pin(t) for t in (qd, kd, vd, out, gd, lse)]
+    klh = torch.from_numpy(kl).pin_memory()
+    devs = [torch.empty_like(t, device=dev) for t in hosts]
+    grads_h = [torch.empty_like(t, device="cpu").pin_memory() for t in (dq, dk, dv)]
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for d_, h_ in zip(devs, hosts):
+            d_.copy_(h_, non_blocking=True)
+        if key_lens is not None:
+            kld.copy_(klh, non_blocking=True)
+        attn.attn_bwd(*devs[:5], devs[5], dq, dk, dv, ws, w.scale, w.mask_mode, key_lens, stream)
+        for h_, d_ in zip(grads_h, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    h2d = sum(t.numel() * t.element_size() for t in hosts) + (klh.numel() * 4 if key_lens is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in grads_h)
+    e2e = {"value": round(weak_scaling_tflops(flops_step, 1, e2e_ms, world), 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
+           "steps": e2e_steps, "how": "pinned host buffers, copies and kernels on one stream, CUDA events"}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    achieved = flops_step / (ms_per_step / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": float(peaks["bf16_tflops"]),
+            "unit": "TFLOP/s", "peak_source": f"bf16_tflops (burst) of {peak_src}",
+            "kernel": "attn_bwd (dot kernel + dK/dV kernel + dQ kernel, timed together)", "traffic": None}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    line = {
+        "metric": "attention bwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, {"pass": "gradients (attn_bwd)",
+                                "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB memset)",
+                                "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 3,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_grad(w, (q, k, v, kl), dout)
+    return line
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, w):
     world, rank, _ = dist_env()
@@ -430,6 +582,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--grad", action="store_true", help="time the gradients (attn_bwd) instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -440,7 +593,14 @@ def main():
     if world != args.gpus:
         if world == 1 and args.gpus > 1:
             ap.error("--gpus N > 1 must be launched with torchrun (one process per GPU)")
-    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if args.grad:
+        if w.mask_mode & (W.MASK_DECODE | W.MASK_WINDOW):
+            ap.error("--grad covers the full-attention workloads (no decode or local-window masks)")
+        if args.impl == "reference":
+            ap.error("--grad is measured for --impl ours; its line carries the oracle's cpu_baseline")
+        line = run_ours_grad(args, w)
+    else:
+        line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None and rank == 0:
         print(json.dumps(line), flush=True)
 

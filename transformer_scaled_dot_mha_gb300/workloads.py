@@ -62,6 +62,12 @@ class Workload:
         """2 (d_k + d_v) FLOPs per legal pair: a d_k-long dot product and a d_v-long axpy."""
         return 2.0 * (self.d_k + self.d_v) * self.legal_pairs(key_lens)
 
+    def algorithmic_bwd_flops(self, key_lens=None) -> float:
+        """Gradients: 2 (3 d_k + 2 d_v) FLOPs per legal pair -- the five products
+        S = Q K^T (d_k), dP = dO V^T (d_v), dV = P^T dO (d_v), dK = dS^T Q and
+        dQ = dS K (d_k each)."""
+        return 2.0 * (3 * self.d_k + 2 * self.d_v) * self.legal_pairs(key_lens)
+
     def dense_flops(self) -> float:
         return 2.0 * (self.d_k + self.d_v) * self.B * self.H * self.n_q * self.n_k
 
@@ -142,6 +148,17 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bf16 (nearest, ties to even); returns uint16 bit patterns."""
     u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
     return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def make_grad_output(w: Workload, seed: int | None = None, **shape) -> np.ndarray:
+    """Draw dout, the gradient arriving at the attention output, [B, H, n_q, d_v]:
+    standard normal float32 from PCG64 seeded with ``seed + 1`` (default: the
+    workload's seed + 1), rounded to bf16 bits for bf16 workloads."""
+    B, H = shape.get("B", w.B), shape.get("H", w.H)
+    n_q, d_v = shape.get("n_q", w.n_q), shape.get("d_v", w.d_v)
+    rng = np.random.Generator(np.random.PCG64((w.seed if seed is None else seed) + 1))
+    x = rng.standard_normal((B, H, n_q, d_v), dtype=np.float32)
+    return to_bf16_bits(x) if w.dtype == "bf16" else x
 
 
 def make_inputs(w: Workload, seed: int | None = None, **shape):
