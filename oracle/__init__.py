@@ -61,8 +61,10 @@ class Oracle:
         self.lib.oracle_attn_rows.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, lp, vp, vp, vp, i]
         self.lib.oracle_attn_weights.argtypes = [vp, vp, i, i, i, i, i, i, d, i, vp, i, vp]
         self.lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, vp, vp, vp, i]
+        self.lib.oracle_mha.argtypes = [vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, vp,
+                                        i]
         for f in (self.lib.oracle_attn, self.lib.oracle_attn_rows, self.lib.oracle_attn_weights,
-                  self.lib.oracle_attn_bwd):
+                  self.lib.oracle_attn_bwd, self.lib.oracle_mha):
             f.restype = ctypes.c_int
 
     @staticmethod
@@ -153,6 +155,42 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_attn_bwd rejected its arguments")
         return dq, dk, dv
+
+    def mha(self, x_q, x_kv, w_q, w_k, w_v, w_o, H, scale=None, mask_mode=MASK_NONE, key_lens=None,
+            b_q=None, b_k=None, b_v=None, b_o=None, n_threads=None):
+        """Multi-head attention ``Y [B, n_q, d_model]`` in float64 (``oracle_mha``).
+
+        ``x_q [B,n_q,d_model]``, ``x_kv [B,n_k,d_model]``; ``w_q, w_k [d_model, H*d_k]``,
+        ``w_v [d_model, H*d_v]``, ``w_o [H*d_v, d_model]`` (the paper's ``x W``
+        orientation); biases optional. All arrays share one dtype. ``scale``
+        defaults to 1/sqrt(d_k) rounded to float32, as the CUDA path uses it."""
+        arrs = [np.ascontiguousarray(a) for a in (x_q, x_kv, w_q, w_k, w_v, w_o)]
+        bias = [None if b is None else np.ascontiguousarray(b) for b in (b_q, b_k, b_v, b_o)]
+        dt = arrs[0].dtype
+        if any(a.dtype != dt for a in arrs + [b for b in bias if b is not None]) or dt not in _DTYPES:
+            raise TypeError("inputs, weights and biases must share one of float64/float32/uint16(bf16)")
+        x_q, x_kv, w_q, w_k, w_v, w_o = arrs
+        B, n_q, d_model = x_q.shape
+        n_k = x_kv.shape[1]
+        d_k, d_v = w_q.shape[1] // H, w_v.shape[1] // H
+        if (x_kv.shape != (B, n_k, d_model) or w_q.shape != (d_model, H * d_k) or w_k.shape != w_q.shape
+                or w_v.shape != (d_model, H * d_v) or w_o.shape != (H * d_v, d_model)):
+            raise ValueError("inconsistent multi-head attention shapes")
+        for b, n in zip(bias, (H * d_k, H * d_k, H * d_v, d_model)):
+            if b is not None and b.shape != (n,):
+                raise ValueError("bias shapes must be [H*d_k], [H*d_k], [H*d_v], [d_model]")
+        if scale is None:
+            scale = float(np.float32(1.0 / np.sqrt(d_k)))
+        kl = self._lens(mask_mode, key_lens, B)
+        y = np.empty((B, n_q, d_model), np.float64)
+        ptr = lambda a: None if a is None else a.ctypes.data
+        rc = self.lib.oracle_mha(x_q.ctypes.data, x_kv.ctypes.data, _DTYPES[dt], w_q.ctypes.data, ptr(bias[0]),
+                                 w_k.ctypes.data, ptr(bias[1]), w_v.ctypes.data, ptr(bias[2]), w_o.ctypes.data,
+                                 ptr(bias[3]), B, n_q, n_k, d_model, H, d_k, d_v, float(scale), int(mask_mode),
+                                 ptr(kl), y.ctypes.data, self._threads(n_threads))
+        if rc != 0:
+            raise ValueError("oracle_mha rejected its arguments")
+        return y
 
     @staticmethod
     def _inputs4(q, k, v, dout):

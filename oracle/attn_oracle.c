@@ -299,3 +299,66 @@ int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dou
   free(th);
   return rc ? -1 : 0;
 }
+
+/* ---------------------------------------------------------------- multi-head attention */
+/* x [B, n, d_in] times the head-i columns of w [d_in, H*d] (+ bias), written head-split
+ * as out [B, H, n, d]. */
+static void project_heads(const void* x, const void* w, const void* bias, int dtype, int B, int n, int d_in, int H,
+                          int d, double* out) {
+  const long long wcols = (long long)H * d;
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < n; ++i) {
+      const long long xrow = ((long long)b * n + i) * d_in;
+      for (int h = 0; h < H; ++h)
+        for (int t = 0; t < d; ++t) {
+          const long long col = (long long)h * d + t;
+          double acc = bias ? elem(bias, dtype, col) : 0.0;
+          for (int c = 0; c < d_in; ++c) acc += elem(x, dtype, xrow + c) * elem(w, dtype, (long long)c * wcols + col);
+          out[(((long long)b * H + h) * n + i) * d + t] = acc;
+        }
+    }
+}
+
+int oracle_mha(const void* x_q, const void* x_kv, int dtype, const void* w_q, const void* b_q, const void* w_k,
+               const void* b_k, const void* w_v, const void* b_v, const void* w_o, const void* b_o, int B, int n_q,
+               int n_k, int d_model, int H, int d_k, int d_v, double scale, int mask_mode, const int* key_lens,
+               double* y, int n_threads) {
+  if (!x_q || !x_kv || !w_q || !w_k || !w_v || !w_o || !y) return -1;
+  if (dtype < ORACLE_F64 || dtype > ORACLE_BF16) return -1;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || H <= 0 || d_k <= 0 || d_v <= 0) return -1;
+  if (mask_mode & (ORACLE_MASK_DECODE | ORACLE_MASK_WINDOW)) return -1;
+  const size_t nq = (size_t)B * H * n_q, nk = (size_t)B * H * n_k;
+  double* qh = (double*)malloc(nq * d_k * sizeof(double));
+  double* kh = (double*)malloc(nk * d_k * sizeof(double));
+  double* vh = (double*)malloc(nk * d_v * sizeof(double));
+  double* oh = (double*)malloc(nq * d_v * sizeof(double));
+  int rc = -1;
+  if (qh && kh && vh && oh) {
+    /* the three linear projections, split into heads: head i uses columns i*d_k.. of W^Q */
+    project_heads(x_q, w_q, b_q, dtype, B, n_q, d_model, H, d_k, qh);
+    project_heads(x_kv, w_k, b_k, dtype, B, n_k, d_model, H, d_k, kh);
+    project_heads(x_kv, w_v, b_v, dtype, B, n_k, d_model, H, d_v, vh);
+    /* scaled dot-product attention per head */
+    rc = oracle_attn(qh, kh, vh, ORACLE_F64, B, H, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens, 0, oh, NULL,
+                     n_threads);
+    if (rc == 0) {
+      /* concatenate the heads along the feature axis (head h fills columns h*d_v..) and
+       * apply the output projection W^O [H*d_v, d_model] */
+      for (int b = 0; b < B; ++b)
+        for (int i = 0; i < n_q; ++i)
+          for (int c = 0; c < d_model; ++c) {
+            double acc = b_o ? elem(b_o, dtype, c) : 0.0;
+            for (int h = 0; h < H; ++h)
+              for (int t = 0; t < d_v; ++t)
+                acc += oh[(((long long)b * H + h) * n_q + i) * d_v + t] *
+                       elem(w_o, dtype, ((long long)h * d_v + t) * d_model + c);
+            y[((long long)b * n_q + i) * d_model + c] = acc;
+          }
+    }
+  }
+  free(qh);
+  free(kh);
+  free(vh);
+  free(oh);
+  return rc;
+}

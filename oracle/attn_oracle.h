@@ -82,6 +82,24 @@ int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dou
                     int mask_mode, const int* key_lens, int window,
                     double* dq, double* dk, double* dv, int n_threads);
 
+/* Multi-head attention (vlmlib.cn "multi-head attention": MultiHead(Q,K,V) =
+ * Concat(head_1..head_h) W^O with head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V); the
+ * csdn blog's MultiHeadAttention: linear projections with biases, split_heads,
+ * attention, transpose back and concatenate, output projection):
+ *   x_q [B, n_q, d_model] (the queries' source), x_kv [B, n_k, d_model] (keys' and
+ *   values' source; the same array for self-attention);
+ *   w_q, w_k [d_model, H*d_k], w_v [d_model, H*d_v], w_o [H*d_v, d_model], row-major
+ *   as in x W (the paper's orientation); W_i^Q is columns i*d_k .. i*d_k + d_k - 1;
+ *   b_q, b_k [H*d_k], b_v [H*d_v], b_o [d_model], each may be NULL (no bias);
+ *   every input has the same dtype; mask_mode/key_lens as oracle_attn (causal and key
+ *   padding only); y [B, n_q, d_model] doubles. Everything is accumulated in fp64
+ *   with no intermediate rounding. Returns 0, or -1 on an invalid argument. */
+int oracle_mha(const void* x_q, const void* x_kv, int dtype, const void* w_q, const void* b_q,
+               const void* w_k, const void* b_k, const void* w_v, const void* b_v,
+               const void* w_o, const void* b_o, int B, int n_q, int n_k, int d_model, int H,
+               int d_k, int d_v, double scale, int mask_mode, const int* key_lens, double* y,
+               int n_threads);
+
 #ifdef __cplusplus
 }
 #endif

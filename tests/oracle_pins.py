@@ -444,4 +444,109 @@ def pin_bwd_shift_invariance_and_dead_keys(orc):
     assert np.all(g[1][1, :, 4:] == 0.0) and np.all(g[2][1, :, 4:] == 0.0)
 
 
+# ---------------------------------------------------------------- multi-head attention
+def _mha_params(seed, B, n_q, n_k, d_model, H, d, bias=True):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x_q = rng.standard_normal((B, n_q, d_model))
+    x_kv = rng.standard_normal((B, n_k, d_model))
+    w = [rng.standard_normal((d_model, H * d)) / math.sqrt(d_model) for _ in range(3)]
+    w_o = rng.standard_normal((H * d, d_model)) / math.sqrt(H * d)
+    b = [rng.standard_normal(H * d) for _ in range(3)] + [rng.standard_normal(d_model)] if bias else [None] * 4
+    return x_q, x_kv, w, w_o, b
+
+
+def _mha(orc, x_q, x_kv, w, w_o, b, H, scale, mode=0, kl=None):
+    return orc.mha(x_q, x_kv, w[0], w[1], w[2], w_o, H, scale, mode, kl, b_q=b[0], b_k=b[1], b_v=b[2], b_o=b[3])
+
+
+def pin_mha_single_head_identity(orc):
+    """One head with identity projections and no biases is scaled dot-product
+    attention itself (vlmlib.cn "multi-head attention" with h = 1, W = I)."""
+    rng = np.random.Generator(np.random.PCG64(60))
+    x = rng.standard_normal((2, 6, 5))
+    eye = np.eye(5)
+    kl = np.array([6, 3], np.int32)
+    for mode in (0, C, P, C | P):
+        y = orc.mha(x, x, eye, eye, eye, eye, 1, 0.4, mode, kl)
+        o, _ = orc.attention(x[:, None], x[:, None], x[:, None], 0.4, mode, kl)
+        assert np.abs(y - o[:, 0]).max() < 1e-13, mode
+
+
+def pin_mha_sum_over_heads(orc):
+    """Concat(head_1..head_h) W^O equals the sum over heads of head_i W^O_i (the
+    block rows of W^O), each head_i = Attention(x_q W_i^Q + b, x_kv W_i^K + b,
+    x_kv W_i^V + b) with W_i the i-th block of columns -- restated per head with
+    explicit slices and the matrix form of the attention, cross shape and masks."""
+    H, d = 3, 4
+    x_q, x_kv, w, w_o, b = _mha_params(61, 2, 5, 7, 10, H, d)
+    kl = np.array([7, 4], np.int32)
+    for mode in (0, P):
+        y = _mha(orc, x_q, x_kv, w, w_o, b, H, 0.5, mode, kl)
+        ref = np.broadcast_to(b[3], y.shape).copy()
+        for h in range(H):
+            cols = slice(h * d, (h + 1) * d)
+            qh, kh, vh = (src @ wi[:, cols] + bi[cols] for src, wi, bi in
+                          ((x_q, w[0], b[0]), (x_kv, w[1], b[1]), (x_kv, w[2], b[2])))
+            head = oracle.attention_matrix_form(qh[:, None], kh[:, None], vh[:, None], 0.5, mode, kl)[0]
+            ref += head[:, 0] @ w_o[cols, :]
+        assert np.abs(y - ref).max() < 1e-12, mode
+
+
+def pin_mha_torch_module(orc):
+    """Library cross-check: torch.nn.MultiheadAttention in float64 with the same
+    weights (its projections are x W^T + b, so it takes our W transposed), key
+    padding and the causal mask."""
+    import torch
+
+    H, d, d_model = 2, 4, 8
+    x_q, x_kv, w, w_o, b = _mha_params(62, 2, 6, 6, d_model, H, d)
+    kl = np.array([6, 4], np.int32)
+    m = torch.nn.MultiheadAttention(d_model, H, bias=True, batch_first=True, dtype=torch.float64)
+    with torch.no_grad():
+        m.in_proj_weight.copy_(torch.from_numpy(np.concatenate([w[0].T, w[1].T, w[2].T])))
+        m.in_proj_bias.copy_(torch.from_numpy(np.concatenate(b[:3])))
+        m.out_proj.weight.copy_(torch.from_numpy(w_o.T))
+        m.out_proj.bias.copy_(torch.from_numpy(b[3]))
+    pad = torch.from_numpy(np.arange(6)[None, :] >= kl[:, None])
+    causal = torch.from_numpy(np.triu(np.ones((6, 6), bool), 1))
+    for mode, kpm, am in ((0, None, None), (P, pad, None), (C, None, causal), (C | P, pad, causal)):
+        with torch.no_grad():
+            t, _ = m(torch.from_numpy(x_q), torch.from_numpy(x_kv), torch.from_numpy(x_kv), key_padding_mask=kpm,
+                     attn_mask=am, need_weights=False)
+        y = _mha(orc, x_q, x_kv, w, w_o, b, H, 1 / math.sqrt(d), mode, kl)
+        assert np.abs(y - t.numpy()).max() < 1e-12, mode
+
+
+def pin_mha_causal_row0_and_head_permutation(orc):
+    """With the causal mask, position 0 sees only itself, so every head returns its
+    value row: Y_0 = (x_0 W^V + b_V) W^O + b_O (closed form). Renumbering the heads
+    (the same permutation of the column blocks of W^Q, W^K, W^V, their biases and
+    the row blocks of W^O) leaves Y unchanged (heads are independent and summed)."""
+    H, d = 4, 3
+    x_q, _, w, w_o, b = _mha_params(63, 2, 5, 5, 9, H, d)
+    y = _mha(orc, x_q, x_q, w, w_o, b, H, 0.6, C)
+    y0 = (x_q[:, 0] @ w[2] + b[2]) @ w_o + b[3]
+    assert np.abs(y[:, 0] - y0).max() < 1e-12
+    perm = [2, 0, 3, 1]
+    idx = np.concatenate([np.arange(h * d, (h + 1) * d) for h in perm])
+    y2 = _mha(orc, x_q, x_q, [wi[:, idx] for wi in w], w_o[idx], [bi[idx] for bi in b[:3]] + [b[3]], H, 0.6, C)
+    assert np.abs(y - y2).max() < 1e-12
+
+
+def pin_mha_bf16_inputs_widen_exactly(orc):
+    """bf16 bit patterns are widened exactly: the same values given as float64 give
+    bit-identical results."""
+    H, d = 2, 4
+    x_q, x_kv, w, w_o, b = _mha_params(64, 1, 4, 6, 8, H, d)
+    bits = lambda a: ((np.asarray(a, np.float32).view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
+    wide = lambda u: (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    args16 = [bits(a) for a in (x_q, x_kv, *w, w_o)]
+    b16 = [bits(x) for x in b]
+    y16 = orc.mha(*args16[:5], args16[5], H, 0.5, P, np.array([5], np.int32),
+                  b_q=b16[0], b_k=b16[1], b_v=b16[2], b_o=b16[3])
+    y64 = orc.mha(*[wide(a) for a in args16], H, 0.5, P, np.array([5], np.int32),
+                  b_q=wide(b16[0]), b_k=wide(b16[1]), b_v=wide(b16[2]), b_o=wide(b16[3]))
+    assert np.array_equal(y16, y64)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

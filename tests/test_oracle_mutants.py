@@ -46,6 +46,15 @@ MUTANTS = {
                       "dq[qoff + (long long)i * p->d_k + t] += p->scale * ds * elem(p->q, p->dtype, qoff + (long long)i * p->d_k + t);"),
     "bwd_dv_unweighted": ("dv[voff + (long long)j * p->d_v + t] += w[j] *", "dv[voff + (long long)j * p->d_v + t] += (w[j] > 0.0) *"),
     "window_off_by_one": ("(j > i + p->window || j < i - p->window)", "(j >= i + p->window || j <= i - p->window)"),
+    # multi-head attention: projections, head split, concatenation, output projection
+    "mha_q_from_kv_source": ("project_heads(x_q, w_q, b_q,", "project_heads(x_kv, w_q, b_q,"),
+    "mha_heads_interleaved": ("const long long col = (long long)h * d + t;", "const long long col = (long long)t * H + h;"),
+    "mha_projection_bias_dropped": ("double acc = bias ? elem(bias, dtype, col) : 0.0;", "double acc = 0.0;"),
+    "mha_output_bias_dropped": ("double acc = b_o ? elem(b_o, dtype, c) : 0.0;", "double acc = 0.0;"),
+    "mha_w_o_transposed": ("elem(w_o, dtype, ((long long)h * d_v + t) * d_model + c)",
+                           "elem(w_o, dtype, (long long)c * H * d_v + (long long)h * d_v + t)"),
+    "mha_concat_batch_head_swapped": ("oh[(((long long)b * H + h) * n_q + i) * d_v + t]",
+                                      "oh[(((long long)h * B + b) * n_q + i) * d_v + t]"),
 }
 
 _CHILD = r"""
