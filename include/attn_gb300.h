@@ -23,8 +23,9 @@
  *     split_heads reshape produces, csdn blog reimplementation):
  *       q   [B, h, n_q, d_k]    k [B, h, n_k, d_k]    v [B, h, n_k, d_v]
  *       out [B, h, n_q, d_v]    lse [B, h, n_q] (float32, optional)
- *   - Every pointer is a DEVICE pointer owned by the caller. The library
- *     allocates no device memory; it neither keeps nor frees the pointers.
+ *   - Every pointer is a DEVICE pointer owned by the caller. The library's own
+ *     kernels allocate no device memory (attn_mha_fwd's GEMMs run on cuBLASLt, whose
+ *     handle it creates once per device); it neither keeps nor frees the pointers.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL
  *     for the legacy default stream) and return before the GPU work finishes.
  *   - scale is used exactly as given; callers normally pass 1/sqrt(d_k) computed
@@ -196,6 +197,44 @@ size_t attn_bwd_workspace_size(int B, int h, int n_q);
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
              int mask_mode, const int32_t* key_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_mha_workspace_size -- bytes of device workspace attn_mha_fwd needs: the
+ * projected Q', K', V' and the concatenated heads (bf16) plus 32 MiB of GEMM
+ * workspace. Returns 0 for an invalid or unsupported shape.
+ */
+size_t attn_mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d);
+
+/*
+ * attn_mha_fwd -- the multi-head attention layer (vlmlib.cn "multi-head attention":
+ * MultiHead(Q,K,V) = Concat(head_1..head_h) W^O, head_i = Attention(Q W_i^Q, K W_i^K,
+ * V W_i^V); the csdn blog's MultiHeadAttention with its linear projections, split_heads
+ * and concatenation), bf16 in and out:
+ *   Q' = x_q W^Q + b_Q, K' = x_kv W^K + b_K, V' = x_kv W^V + b_V     [B, n, h*d]
+ *   A  = attn_fwd(Q', K', V') per head, heads concatenated          [B, n_q, h*d]
+ *   out = A W^O + b_O                                                [B, n_q, d_model]
+ *   x_q  [B, n_q, d_model], x_kv [B, n_k, d_model] (pass x_q twice for self-attention)
+ *   w_q, w_k, w_v [d_model, h*d], w_o [h*d, d_model]: row-major, the paper's x W
+ *           orientation (an nn.Linear weight is the transpose); head i uses columns
+ *           i*d .. i*d + d - 1 of W^Q, W^K, W^V and rows i*d .. of W^O
+ *   b_q, b_k, b_v [h*d], b_o [d_model]: bf16 or NULL for no bias
+ *   out  [B, n_q, d_model] bf16
+ *   mask_mode, key_lens, scale: as attn_fwd (scale is normally 1/sqrt(d)).
+ *   workspace: device scratch of at least attn_mha_workspace_size(...) bytes, 16-byte
+ *           aligned, owned by the caller, contents undefined on return; concurrent
+ *           calls must not share it.
+ * Supported: d_k == d_v in {64, 128}, d_model a multiple of 8; every pointer 16-byte
+ * aligned. The four projections run on cuBLASLt (bf16 GEMMs, fp32 accumulation,
+ * bias in the GEMM epilogue, results rounded to bf16); the attention is the attn_fwd
+ * kernel reading Q', K', V' and writing A in their [B, n, h*d] layout, so splitting
+ * and concatenating the heads moves no data. The first call on a device creates a
+ * cuBLASLt handle and, for each new shape, a GEMM plan (host-side, cached). Five
+ * launches on `stream`.
+ */
+int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void* b_q, const void* w_k,
+                 const void* b_k, const void* w_v, const void* b_v, const void* w_o, const void* b_o, void* out,
+                 int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v, float scale, int mask_mode,
+                 const int32_t* key_lens, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_fault_status -- synchronises `stream`, then reports whether any kernel of

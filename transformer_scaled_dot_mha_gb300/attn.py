@@ -53,6 +53,10 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, ctypes.c_size_t,
                                vp]
         L.attn_bwd.restype = i
+        L.attn_mha_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.attn_mha_workspace_size.restype = ctypes.c_size_t
+        L.attn_mha_fwd.argtypes = [vp] * 11 + [i, i, i, i, i, i, i, f, i, vp, vp, ctypes.c_size_t, vp]
+        L.attn_mha_fwd.restype = i
         L.attn_fault_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_uint32)]
         L.attn_fault_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -237,6 +241,44 @@ def attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, scale=None, mask_mo
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_mha_workspace_size(B, n_q, n_k, d_model, H, d) -> int:
+    return int(lib().attn_mha_workspace_size(B, n_q, n_k, d_model, H, d))
+
+
+def attn_mha_fwd(x_q, x_kv, w_q, w_k, w_v, w_o, out, H, workspace, b_q=None, b_k=None, b_v=None, b_o=None,
+                 scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
+    """Multi-head attention layer into caller-provided ``out [B, n_q, d_model]`` (bf16):
+    ``x_q [B,n_q,d_model]``, ``x_kv [B,n_k,d_model]``, ``w_q, w_k, w_v [d_model, H*d]``,
+    ``w_o [H*d, d_model]`` (the paper's x W orientation), optional biases, and a CUDA
+    ``workspace`` of at least ``attn_mha_workspace_size`` bytes."""
+    for t, n in ((x_q, "x_q"), (x_kv, "x_kv"), (out, "out")):
+        _check(t, n, torch.bfloat16, 3)
+    for t, n in ((w_q, "w_q"), (w_k, "w_k"), (w_v, "w_v"), (w_o, "w_o")):
+        _check(t, n, torch.bfloat16, 2)
+    for t, n in ((b_q, "b_q"), (b_k, "b_k"), (b_v, "b_v"), (b_o, "b_o")):
+        if t is not None:
+            _check(t, n, torch.bfloat16, 1)
+    B, n_q, d_model = x_q.shape
+    n_k = x_kv.shape[1]
+    d_k, d_v = w_q.shape[1] // H, w_v.shape[1] // H
+    if (x_kv.shape != (B, n_k, d_model) or w_q.shape != (d_model, H * d_k) or w_k.shape != w_q.shape
+            or w_v.shape != (d_model, H * d_v) or w_o.shape != (H * d_v, d_model) or out.shape != x_q.shape):
+        raise ValueError("inconsistent multi-head attention shapes")
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, 1)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib().attn_mha_fwd(_ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(b_q), _ptr(w_k), _ptr(b_k), _ptr(w_v), _ptr(b_v),
+                            _ptr(w_o), _ptr(b_o), _ptr(out), B, n_q, n_k, d_model, H, d_k, d_v, float(scale),
+                            int(mask_mode), _ptr(key_lens), _ptr(workspace), nbytes, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_mha_fwd")
+    return out
 
 
 def attn_fault_status(stream=None, clear=True):

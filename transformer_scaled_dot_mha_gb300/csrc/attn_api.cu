@@ -148,6 +148,36 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   return attn::launch_attn_bwd(a, enc, workspace);
 }
 
+size_t attn_mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d) {
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || (d != 64 && d != 128)) return 0;
+  if ((long long)B * (n_q > n_k ? n_q : n_k) * h * d > (1LL << 38)) return 0;
+  return attn::mha_workspace_bytes(B, n_q, n_k, h, d);
+}
+
+int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void* b_q, const void* w_k,
+                 const void* b_k, const void* w_v, const void* b_v, const void* w_o, const void* b_o, void* out,
+                 int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v, float scale, int mask_mode,
+                 const int32_t* key_lens, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x_q || !x_kv || !w_q || !w_k || !w_v || !w_o || !out || !workspace) return ATTN_ERR_INVALID;
+  if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_k <= 0 || d_v <= 0) return ATTN_ERR_INVALID;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID;
+  if (mask_mode < 0 || mask_mode > (ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return ATTN_ERR_INVALID;
+  if ((mask_mode & ATTN_MASK_CAUSAL) && n_q != n_k) return ATTN_ERR_INVALID;
+  if ((mask_mode & ATTN_MASK_KEY_PADDING) && (!key_lens || !aligned(key_lens, 4))) return ATTN_ERR_INVALID;
+  const void* ptrs16[] = {x_q, x_kv, w_q, w_k, w_v, w_o, out, workspace, b_q, b_k, b_v, b_o};
+  for (const void* ptr : ptrs16)
+    if (ptr && !aligned(ptr, 16)) return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128) || d_model % 8 != 0) return ATTN_ERR_UNSUPPORTED;
+  const size_t need = attn_mha_workspace_size(B, n_q, n_k, d_model, h, d_k);
+  if (need == 0) return ATTN_ERR_INVALID;
+  if (workspace_bytes < need) return ATTN_ERR_INVALID;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::MhaArgs a{x_q, x_kv, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, out, B, n_q, n_k, d_model, h, d_k, scale,
+                  mask_mode, key_lens, static_cast<cudaStream_t>(stream)};
+  return attn::launch_attn_mha(a, enc, workspace);
+}
+
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code) {
   uint32_t w = 0, wb = 0;
   const int st = attn::read_fault_word(static_cast<cudaStream_t>(stream), clear, &w);

@@ -168,9 +168,21 @@ __device__ __forceinline__ void tile_range(int r0, int n_q, int kv_len, bool cau
   n = (hi + BN - 1) / BN - jb;
 }
 
+// First element of output row i of head bh (batch b) in either layout.
+template <int D, bool HEADS_INTERLEAVED>
+__device__ __forceinline__ uint16_t* out_row_of(const Params& p, int b, int bh, int i) {
+  if constexpr (HEADS_INTERLEAVED)
+    return p.out + (((size_t)b * p.n_q + i) * p.H + (bh - b * p.H)) * D;
+  else
+    return p.out + ((size_t)bh * p.n_q + i) * D;
+}
+
 // LOCAL: local-window instantiation (attn_fwd_local). The plain instantiation sees a
 // constant window of -1, so its tile ranges start at tile 0 and fold to constants.
-template <int D, bool LOCAL>
+// HEADS_INTERLEAVED: Q, K, V and out are [B, n, h*d] (the projections' own layout,
+// before split_heads / after the concatenation of the heads) instead of [B, h, n, d];
+// the tensor maps then span (h*d, n, B) and a head is an x offset of h*d.
+template <int D, bool LOCAL, bool HEADS_INTERLEAVED>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -190,6 +202,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const int bh = blockIdx.x % p.BH;
   const int qb = p.num_qblocks - 1 - blockIdx.x / p.BH;
   const int b = bh / p.H;
+  const int tma_z = HEADS_INTERLEAVED ? b : bh;                   // TMA z coordinate of this head
+  const int tma_x = HEADS_INTERLEAVED ? (bh - b * p.H) * D : 0;  // and its x offset
   const int row0 = qb * 2 * BM;
   const bool causal = (p.mask_mode & 1) != 0;
   int kv_len = p.n_k;
@@ -254,8 +268,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       ptx::mbar_arrive_expect_tx(bar(C::B_QFULL), n_qt * C::TILE_BYTES);
       for (int t = 0; t < n_qt; ++t)
         for (int c = 0; c < C::CHUNKS; ++c)
-          ptx::tma_load_3d(s_q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL), c * 64,
-                           row0 + t * BM, bh, pol_q);
+          ptx::tma_load_3d(s_q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL), tma_x + c * 64,
+                           row0 + t * BM, tma_z, pol_q);
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < n_max && ok; ++j) {
@@ -265,8 +279,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c)
-          ptx::tma_load_3d(s_k + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + s), c * 64,
-                           (J0 + j) * BN, bh, pol_kv);
+          ptx::tma_load_3d(s_k + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + s),
+                           tma_x + c * 64, (J0 + j) * BN, tma_z, pol_kv);
         ok = wait_bar(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER);
         if (!ok) {
           issued = 2 * j + 1;
@@ -274,8 +288,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
         ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c)
-          ptx::tma_load_3d(s_v + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bar(C::B_VFULL + s), c * 64,
-                           (J0 + j) * BN, bh, pol_kv);
+          ptx::tma_load_3d(s_v + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bar(C::B_VFULL + s),
+                           tma_x + c * 64, (J0 + j) * BN, tma_z, pol_kv);
         issued = 2 * j + 2;
       }
       if (!ok) {
@@ -593,7 +607,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       if (ok) {
         ptx::tc_fence_after();
         const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-        uint16_t* orow = p.out + ((size_t)bh * p.n_q + (size_t)(row_valid ? i : 0)) * D;
+        uint16_t* orow = out_row_of<D, HEADS_INTERLEAVED>(p, b, bh, row_valid ? i : 0);
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
           uint32_t o[32];
@@ -614,7 +628,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
     } else if (ok && row_valid) {
       // no legal key at all (key length 0): o = 0, lse = -inf
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.n_q + i) * D);
+      uint4* dst = reinterpret_cast<uint4*>(out_row_of<D, HEADS_INTERLEAVED>(p, b, bh, i));
 #pragma unroll
       for (int x = 0; x < D / 8; ++x) dst[x] = make_uint4(0, 0, 0, 0);
       if (p.lse) p.lse[(size_t)bh * p.n_q + i] = -INFINITY;
@@ -640,7 +654,20 @@ CUresult encode_map(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D, bool LOCAL>
+// [B, n, h*d]: the map spans (h*d, n, B); a head's tile is read at x = h*d + 64c.
+CUresult encode_map_interleaved(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int d, int H, int n,
+                                int B) {
+  const cuuint64_t row = (cuuint64_t)H * d;
+  cuuint64_t dims[3] = {row, (cuuint64_t)n, (cuuint64_t)B};
+  cuuint64_t strides[2] = {row * 2, row * 2 * (cuuint64_t)n};
+  cuuint32_t box[3] = {64, (cuuint32_t)BM, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int D, bool LOCAL, bool HEADS_INTERLEAVED>
 int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv) {
   using C = Cfg<D>;
   // the shared-memory opt-in is per device; set it once for each device used
@@ -648,7 +675,7 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_done[dev].store(true, std::memory_order_release);
@@ -667,18 +694,27 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   const long long grid = (long long)p.BH * p.num_qblocks;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_fwd_tc_kernel<D, LOCAL><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv,
+                                                                                                         p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 template <int D>
 int launch(const TcArgs& a, PFN_encodeTiled enc) {
   CUtensorMap mq, mk, mv;
+  if (a.heads_interleaved) {
+    if (a.window >= 0) return ATTN_ERR_UNSUPPORTED;
+    if (encode_map_interleaved(enc, &mq, a.q, D, a.H, a.n_q, a.B) != CUDA_SUCCESS ||
+        encode_map_interleaved(enc, &mk, a.k, D, a.H, a.n_k, a.B) != CUDA_SUCCESS ||
+        encode_map_interleaved(enc, &mv, a.v, D, a.H, a.n_k, a.B) != CUDA_SUCCESS)
+      return ATTN_ERR_UNSUPPORTED;
+    return launch_variant<D, false, true>(a, mq, mk, mv);
+  }
   if (encode_map(enc, &mq, a.q, D, a.n_q, a.B * a.H) != CUDA_SUCCESS ||
       encode_map(enc, &mk, a.k, D, a.n_k, a.B * a.H) != CUDA_SUCCESS ||
       encode_map(enc, &mv, a.v, D, a.n_k, a.B * a.H) != CUDA_SUCCESS)
     return ATTN_ERR_UNSUPPORTED;
-  return a.window >= 0 ? launch_variant<D, true>(a, mq, mk, mv) : launch_variant<D, false>(a, mq, mk, mv);
+  return a.window >= 0 ? launch_variant<D, true, false>(a, mq, mk, mv) : launch_variant<D, false, false>(a, mq, mk, mv);
 }
 
 }  // namespace

@@ -28,6 +28,7 @@ struct TcArgs {
   const int32_t* key_lens;
   cudaStream_t stream;
   int window;  // local-window radius (>= 0), or -1 for none
+  int heads_interleaved = 0;  // 1: q, k, v, out are [B, n, H*d] instead of [B, H, n, d]
 };
 
 // Validated arguments of one fp32 call.
@@ -75,6 +76,26 @@ struct BwdArgs {
   cudaStream_t stream;
 };
 
+// Validated arguments of one multi-head layer call (d_k == d_v == d).
+struct MhaArgs {
+  const void* x_q;
+  const void* x_kv;
+  const void* w_q;
+  const void* b_q;
+  const void* w_k;
+  const void* b_k;
+  const void* w_v;
+  const void* b_v;
+  const void* w_o;
+  const void* b_o;
+  void* out;
+  int B, n_q, n_k, d_model, H, d;
+  float scale;
+  int mask_mode;
+  const int32_t* key_lens;
+  cudaStream_t stream;
+};
+
 int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc);   // attn_fwd_tc.cu
 int launch_attn_f32(const F32Args& a);                       // attn_fwd_f32.cu
 int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd_tc.cu
@@ -86,5 +107,7 @@ int read_decode_fault_word(int clear, uint32_t* out);                   // attn_
 size_t bwd_workspace_bytes(int B, int H, int n_q);                       // attn_bwd.cu
 int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_bwd.cu
 int read_bwd_fault_word(int clear, uint32_t* out);                       // attn_bwd.cu
+size_t mha_workspace_bytes(int B, int n_q, int n_k, int H, int d);         // attn_mha.cu
+int launch_attn_mha(const MhaArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_mha.cu
 
 }  // namespace attn

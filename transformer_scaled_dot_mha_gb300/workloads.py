@@ -161,6 +161,32 @@ def make_grad_output(w: Workload, seed: int | None = None, **shape) -> np.ndarra
     return to_bf16_bits(x) if w.dtype == "bf16" else x
 
 
+def make_mha_inputs(w: Workload, seed: int | None = None, d_model: int | None = None, bias: bool = True, **shape):
+    """Draw a multi-head layer's inputs for workload ``w`` (bf16 bits, uint16):
+    x_q [B, n_q, d_model] and x_kv [B, n_k, d_model] standard normal; W^Q, W^K, W^V
+    [d_model, H*d] and W^O [H*d, d_model] normal with variance 1/(rows) so every
+    projection has unit variance; biases normal x 0.1 (None when ``bias`` is False);
+    then key lengths as in ``make_inputs``. PCG64 seeded with ``seed + 2`` (default
+    the workload's seed + 2); d_model defaults to H*d (the pages' d_model = h d_k)."""
+    B, H = shape.get("B", w.B), shape.get("H", w.H)
+    n_q, n_k, d = shape.get("n_q", w.n_q), shape.get("n_k", w.n_k), shape.get("d_k", w.d_k)
+    d_model = H * d if d_model is None else d_model
+    rng = np.random.Generator(np.random.PCG64((w.seed if seed is None else seed) + 2))
+    nrm = lambda shp, sc=1.0: to_bf16_bits(rng.standard_normal(shp, dtype=np.float32) * np.float32(sc))
+    x_q, x_kv = nrm((B, n_q, d_model)), nrm((B, n_k, d_model))
+    w_q, w_k, w_v = (nrm((d_model, H * d), 1 / math.sqrt(d_model)) for _ in range(3))
+    w_o = nrm((H * d, d_model), 1 / math.sqrt(H * d))
+    biases = [nrm((H * d,), 0.1) for _ in range(3)] + [nrm((d_model,), 0.1)] if bias else [None] * 4
+    if w.mask_mode & MASK_KEY_PADDING:
+        lo, hi = w.key_len_range
+        key_lens = rng.integers(min(lo, n_k), min(hi, n_k), size=B, endpoint=True).astype(np.int32)
+    else:
+        key_lens = np.full((B,), n_k, np.int32)
+    return {"x_q": x_q, "x_kv": x_kv, "w_q": w_q, "w_k": w_k, "w_v": w_v, "w_o": w_o, "b_q": biases[0],
+            "b_k": biases[1], "b_v": biases[2], "b_o": biases[3], "key_lens": key_lens, "H": H, "d": d,
+            "d_model": d_model}
+
+
 def make_inputs(w: Workload, seed: int | None = None, **shape):
     """Draw (q, k, v, key_lens) for a workload.
 
