@@ -10,6 +10,12 @@ lse stores). FLOPs are algorithmic: 2 (d_k + d_v) per legal query-key pair.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-cpu-baseline] [--grad]
 
+--mha times the whole multi-head attention layer instead (one attn_mha_fwd call per
+step: the Q, K, V projections, the attention on the projections' [B, n, h*d] layout
+and the output projection; d_model = h*d, random weights resident on the device);
+FLOPs are algorithmic: 2 d_model h d per projected row for each of the four
+projections plus the attention's.
+
 --grad times the gradients instead (one attn_bwd call per step: D = rowsum(dO*O),
 the dK/dV kernel and the dQ kernel), given the forward's output and lse computed
 once before the timed region; FLOPs are algorithmic, 2 (3 d_k + 2 d_v) per legal
@@ -527,6 +533,7 @@ def run_ours_grad(args, w):
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, {"pass": "gradients (attn_bwd)",
+                                "flops": "algorithmic: 2*(3*d_k+2*d_v) per legal (query, key) pair",
                                 "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB memset)",
                                 "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
         "roofline": roof,
@@ -537,6 +544,174 @@ def run_ours_grad(args, w):
     }
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_grad(w, (q, k, v, kl), dout)
+    return line
+
+
+# ---------------------------------------------------------------- multi-head layer
+def mha_flops(w, key_lens):
+    hd, d_model = w.H * w.d_k, w.H * w.d_k
+    proj = 2.0 * d_model * hd * w.B * (2 * w.n_q + 2 * w.n_k)
+    return proj + w.algorithmic_flops(key_lens)
+
+
+def cpu_baseline_mha(w, target_s=12.0):
+    """The oracle's multi-head layer, as it stands, on a bounded sample: one batch
+    row of the same layer (d_model, h, d, mask) with a shortened sequence, grown
+    until it takes about ``target_s`` seconds."""
+    import oracle
+
+    if not os.path.exists(oracle.LIB):
+        oracle.build()
+    orc = oracle.Oracle()
+    threads = os.cpu_count() or 1
+    n = 16
+    while True:
+        inp = W.make_mha_inputs(w, B=1, n_q=n, n_k=n if w.n_q == w.n_k else 2 * n)
+        kl = np.minimum(inp["key_lens"], inp["x_kv"].shape[1])
+        t0 = time.perf_counter()
+        orc.mha(inp["x_q"], inp["x_kv"], inp["w_q"], inp["w_k"], inp["w_v"], inp["w_o"], w.H, w.scale, w.mask_mode,
+                kl, b_q=inp["b_q"], b_k=inp["b_k"], b_v=inp["b_v"], b_o=inp["b_o"], n_threads=threads)
+        dt = time.perf_counter() - t0
+        if dt > target_s / 4 or 2 * n > w.n_q:
+            break
+        n *= 2
+    n_k = inp["x_kv"].shape[1]
+    sub = W.Workload(w.name, 1, w.H, n, n_k, w.d_k, w.d_v, w.dtype, w.mask_mode, w.key_len_range, w.input_scale,
+                     w.index, w.window)
+    flops = mha_flops(sub, kl)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"one batch row of the same layer with n_q = {n}, n_k = {n_k} (d_model {w.H * w.d_k}, h {w.H}), "
+                      f"fp64 C oracle (projections single-threaded, attention on {threads} threads), {dt:.2f} s wall"}
+
+
+def run_ours_mha(args, w):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from transformer_scaled_dot_mha_gb300 import attn
+
+    attn.lib()
+    inp = W.make_mha_inputs(w, shard_seed(w, rank))
+    self_attn = w.n_q == w.n_k
+    to_dev = lambda a: None if a is None else torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    xq = to_dev(inp["x_q"])
+    xkv = xq if self_attn else to_dev(inp["x_kv"])
+    wts = {k: to_dev(inp[k]) for k in ("w_q", "w_k", "w_v", "w_o", "b_q", "b_k", "b_v", "b_o")}
+    kl = inp["key_lens"]
+    kld = torch.from_numpy(kl).to(dev)
+    key_lens = kld if w.mask_mode & W.MASK_KEY_PADDING else None
+    d_model = w.H * w.d_k
+    out = torch.empty((w.B, w.n_q, d_model), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(attn.attn_mha_workspace_size(w.B, w.n_q, w.n_k, d_model, w.H, w.d_k), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def layer(x_q, x_kv):
+        attn.attn_mha_fwd(x_q, x_kv, wts["w_q"], wts["w_k"], wts["w_v"], wts["w_o"], out, w.H, ws, wts["b_q"],
+                          wts["b_k"], wts["b_v"], wts["b_o"], w.scale, w.mask_mode, key_lens, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer(xq, xkv)
+    torch.cuda.synchronize()
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} during warm-up")
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        layer(xq, xkv)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop() if rank == 0 else None
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), dev)
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} in the timed region")
+    flops_step = mha_flops(w, kl)
+    ms_per_step = total_ms / args.steps
+    value = weak_scaling_tflops(flops_step, args.steps, total_ms, world)
+
+    # end to end: the layer's inputs from pinned host memory, its output back; the
+    # weights are the model's parameters and stay on the device
+    xqh = xq.cpu().pin_memory()
+    xkvh = xqh if self_attn else xkv.cpu().pin_memory()
+    klh = torch.from_numpy(kl).pin_memory()
+    outh = torch.empty_like(out, device="cpu").pin_memory()
+    xq2 = torch.empty_like(xq)
+    xkv2 = xq2 if self_attn else torch.empty_like(xkv)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        xq2.copy_(xqh, non_blocking=True)
+        if not self_attn:
+            xkv2.copy_(xkvh, non_blocking=True)
+        if key_lens is not None:
+            kld.copy_(klh, non_blocking=True)
+        layer(xq2, xkv2)
+        outh.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    h2d = xqh.numel() * 2 + (0 if self_attn else xkvh.numel() * 2) + (klh.numel() * 4 if key_lens is not None else 0)
+    e2e = {"value": round(weak_scaling_tflops(flops_step, 1, e2e_ms, world), 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(outh.numel() * 2), "ms_per_step": round(e2e_ms, 4),
+           "steps": e2e_steps, "how": "pinned host x in, y out, copies and kernels on one stream, CUDA events; "
+                                     "weights resident on the device"}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    achieved = flops_step / (ms_per_step / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": float(peaks["bf16_tflops"]),
+            "unit": "TFLOP/s", "peak_source": f"bf16_tflops (burst) of {peak_src}",
+            "kernel": "attn_mha_fwd (four cuBLASLt GEMMs + the attention kernel, timed together)", "traffic": None}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    line = {
+        "metric": "multi-head attention layer TFLOP/s on 1 GB300 and % of dense bf16 tensor peak",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, {"pass": "multi-head layer (attn_mha_fwd)", "d_model": d_model,
+                                "inputs": f"x N(0,1), W N(0,1/rows), b N(0,1) x 0.1, seed {w.seed + 2}",
+                                "flops": "algorithmic: four projections 2*d_model*h*d per row + attention",
+                                "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB memset)",
+                                "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 5,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_mha(w)
     return line
 
 
@@ -583,6 +758,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--grad", action="store_true", help="time the gradients (attn_bwd) instead of the forward")
+    ap.add_argument("--mha", action="store_true", help="time the multi-head layer (attn_mha_fwd) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -593,7 +769,13 @@ def main():
     if world != args.gpus:
         if world == 1 and args.gpus > 1:
             ap.error("--gpus N > 1 must be launched with torchrun (one process per GPU)")
-    if args.grad:
+    if args.mha:
+        if args.grad or w.mask_mode & (W.MASK_DECODE | W.MASK_WINDOW):
+            ap.error("--mha covers the forward of the full-attention workloads")
+        if args.impl == "reference":
+            ap.error("--mha is measured for --impl ours; its line carries the oracle's cpu_baseline")
+        line = run_ours_mha(args, w)
+    elif args.grad:
         if w.mask_mode & (W.MASK_DECODE | W.MASK_WINDOW):
             ap.error("--grad covers the full-attention workloads (no decode or local-window masks)")
         if args.impl == "reference":

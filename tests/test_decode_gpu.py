@@ -3,7 +3,7 @@ oracle's decode mask, element by element on the same bf16-rounded inputs.
 
 Tolerance: max |err| <= 1e-2, mean |err| <= 1e-3, lse |err| <= 1e-3 -- the same
 bar as the bf16 forward path (this kernel keeps the weights in fp32, so its only
-bf16 rounding is the output's, 2^-9 relative).
+bf16 rounding is the output's, at most 2^-8 relative).
 """
 import numpy as np
 import pytest

@@ -3,8 +3,10 @@
 Tolerances (against the oracle run on the very same bf16-rounded inputs):
   bf16 path: max |err| <= 1e-2 and mean |err| <= 1e-3 on the output; |err| <= 1e-3
              on lse (natural log). The kernel rounds the softmax weights to bf16
-             before the PV product (relative error <= 2^-9 per weight) and rounds
-             the output to bf16 (<= 2^-9 relative), so for unit-variance V the
+             before the PV product (relative error <= 2^-8 per weight: bf16 keeps 8
+             significant bits, so one rounding to nearest is off by at most 2^-8 of
+             the value) and rounds the output to bf16 (<= 2^-8 relative); these
+             errors are independent across weights, so for unit-variance V the
              expected max error is a few 1e-3.
   fp32 path: max |err| <= 1e-5 (float32 dot products and sums of at most a few
              hundred terms).
@@ -165,11 +167,12 @@ def test_bf16_large_scores_rescaling(orc):
     q2 = W.to_bf16_bits((oracle.widen(q) * 3).astype(np.float32))
     out, lse = run_bf16(q2, k2, v, kl, w.scale, 0)
     ref, ref_lse = orc.attention(q2, k2, v, w.scale, 0)
-    # Sharp rows are dominated by a few weights, so the bf16 rounding of P (relative
-    # 2^-9 per weight) and of the output (2^-9 |o|) no longer average out; together
-    # they are bounded by 2^-8 max|V|, which is the bound used here.
+    # Sharp rows are dominated by a few weights, so the bf16 rounding of P (at most
+    # 2^-8 of each weight, and the weights sum to 1) and of the output (2^-8 |o|) no
+    # longer average out; together they are bounded by 2 * 2^-8 max|V| = 2^-7 max|V|,
+    # which is the bound used here.
     err = np.abs(out - ref)
-    assert err.max() <= 2.0 ** -8 * np.abs(oracle.widen(v)).max() and err.mean() <= BF16_MEAN
+    assert err.max() <= 2.0 ** -7 * np.abs(oracle.widen(v)).max() and err.mean() <= BF16_MEAN
     assert np.abs(lse - ref_lse).max() <= LSE_TOL
 
 
