@@ -74,6 +74,105 @@ def kernel_source_hash(kernel: str = "attn_fwd_tc_kernel") -> str:
     return h.hexdigest()[:16]
 
 
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_seed(w, rank: int) -> int:
+    """Each rank draws its own shard of (b, h) problems; rank 0 keeps the workload's seed."""
+    return w.seed + 1000 * rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a per-rank scalar over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tflops(flops_per_rank_step: float, steps: int, max_total_ms: float, world: int) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (max_total_ms / 1e3) / 1e12
+
+
+def mask_name(mode):
+    names = {1: "causal", 2: "key_padding", 4: "decode", 8: "window"}
+    return "+".join(v for k, v in names.items() if mode & k) or "none"
+
+
+def config_of(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "h": w.H, "n_q": w.n_q, "n_k": w.n_k, "d_k": w.d_k, "d_v": w.d_v,
+           "mask": mask_name(w.mask_mode), "inputs": f"N(0,1) x {w.input_scale}, seed {w.seed}",
+           **({"window": w.window} if w.mask_mode & W.MASK_WINDOW else {}),
+           "flops": "algorithmic: 2*(d_k+d_v) per legal (query, key) pair"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for ln in out.splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) == 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples arrive every 100 ms; keep the loaded ones (the timed region is short)
+        loaded = [r for r in rows if float(r[3]) > 200.0] or rows
+        sm = [float(r[1]) for r in loaded]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(float(r[2]) for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded), "power_w_max": max(float(r[3]) for r in loaded)}
+
+
 # ---------------------------------------------------------------- CPU oracle leg
 def sample_row_ids(w, rng_seed=7):
     """Row ids spread over all heads and positions of the workload."""
