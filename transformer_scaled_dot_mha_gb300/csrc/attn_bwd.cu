@@ -43,8 +43,11 @@ __device__ unsigned int g_bwd_fault_word;  // fault record of the gradient kerne
 namespace {
 
 constexpr int T = 128;          // rows per tile (queries or keys)
-constexpr int THREADS = 192;    // warps 0-3 elementwise, 4 producer, 5 MMA issuer
-constexpr int WARP_LOAD = 4, WARP_MMA = 5;
+// warps 0-7 elementwise (two warpgroups, one per half of the streamed tile's 128
+// columns), warp 8 TMA producer, warp 9 MMA issuer
+constexpr int EW_THREADS = 256;
+constexpr int THREADS = EW_THREADS + 64;
+constexpr int WARP_LOAD = 8, WARP_MMA = 9;
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
@@ -63,7 +66,7 @@ struct BCfg {
   static constexpr int OFF_A1 = OFF_A0 + TILE_BYTES;        // V (dkdv) or dO (dq)
   static constexpr int OFF_R0 = OFF_A1 + TILE_BYTES;        // ring: Q_i (dkdv) or K_j (dq)
   static constexpr int OFF_R1 = OFF_R0 + STAGES * TILE_BYTES;  // ring: dO_i (dkdv) or V_j (dq)
-  static constexpr int OFF_VEC = OFF_R1 + STAGES * TILE_BYTES;  // float lse[STAGES][T], dd[STAGES][T]
+  static constexpr int OFF_VEC = OFF_R1 + STAGES * TILE_BYTES;  // float -lse*log2e[STAGES][T], -D[STAGES][T]
   static constexpr int OFF_BAR = OFF_VEC + 2 * STAGES * T * 4;
   // barriers: a_full, full[S], empty[S], mm_full, p_full, acc_done, drain
   static constexpr int B_AFULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_MMFULL = B_EMPTY + STAGES;
@@ -71,7 +74,10 @@ struct BCfg {
   static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_SLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
-  // TMEM: X [0,128) = S^T or S, Y [128,256) = dP^T or dP, acc0 [256, 256+D), acc1 [256+D, 256+2D)
+  // TMEM: X [0,128) = S^T or S, Y [128,256) = dP^T or dP, acc0 [256, 256+D), acc1 [256+D, 256+2D).
+  // The bf16 pairs written back over X and Y (P^T / dS^T, or dS) sit in columns
+  // [0, 32) for streamed rows 0-63 and [64, 96) for rows 64-127 of their region: each
+  // elementwise warpgroup writes only over columns it has already read.
   static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
   static constexpr uint32_t IDESC_NN = ptx::idesc_bf16_f32(T, T, false);  // both operands K-major
   static constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(T, D, true);  // B MN-major
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(bar(C::B_EMPTY + s), 1);
     }
     ptx::mbar_init(bar(C::B_MMFULL), 1);
-    ptx::mbar_init(bar(C::B_PFULL), T);
+    ptx::mbar_init(bar(C::B_PFULL), EW_THREADS);
     ptx::mbar_init(bar(C::B_ACC), 1);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -224,12 +230,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         if (DKDV) {
-          // lse and D of the 128 queries of this tile (rows past n_q: lse = +inf -> P = 0)
+          // -lse*log2e and -D of the 128 queries of this tile (rows past n_q get
+          // -inf, so their P is 0)
           for (int x = lane; x < T; x += 32) {
             const int i = r0 + x;
             const bool in = i < p.n_q;
-            vec[st * T + x] = in ? p.lse[(size_t)bh * p.n_q + i] : INFINITY;
-            vec[(STAGES + st) * T + x] = in ? p.dd[(size_t)bh * p.n_q + i] : 0.0f;
+            vec[st * T + x] = in ? -p.lse[(size_t)bh * p.n_q + i] * 1.4426950408889634f : -INFINITY;
+            vec[(STAGES + st) * T + x] = in ? -p.dd[(size_t)bh * p.n_q + i] : 0.0f;
           }
           ptx::mbar_arrive(bar(C::B_FULL + st));
         }
@@ -273,13 +280,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         // dQ:   dQ += dS K_j (dS over X), B = R0 MN-major
 #pragma unroll
         for (int kk = 0; kk < T / 16; ++kk) {
+          const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // bf16 pairs of streamed rows 16kk..16kk+15
           if (DKDV) {
-            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::TM_X + kk * 8, ptx::sdesc_sw128(r1 + kk * 2048, C::CHUNK_BYTES, 1024),
+            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::TM_X + a_col, ptx::sdesc_sw128(r1 + kk * 2048, C::CHUNK_BYTES, 1024),
                         C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_Y + kk * 8, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_Y + a_col, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
                         C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
           } else {
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_X + kk * 8, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_X + a_col, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
                         C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
           }
         }
@@ -293,20 +301,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ================================================================ elementwise warpgroup
-    const int r = warp * 32 + lane;  // TMEM lane = own row (key for DKDV, query for dQ)
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ================================================================ elementwise warpgroups
+    // Thread = own row (key for DKDV, query for dQ) = TMEM lane; warpgroup g takes the
+    // streamed tile's columns [64g, 64g + 64). No element needs another: P and dS of
+    // one (key, query) pair use only that pair's S, dP and the query's lse and D.
+    const int g = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_x = tmem + lane_off + C::TM_X + g * 64, t_y = tmem + lane_off + C::TM_Y + g * 64;
     const int own_row = own0 + r;
-    const float c = p.scale_log2;
-    const float LOG2E = 1.4426950408889634f;
+    const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     // dQ: this thread's query statistics
-    float my_lse2 = 0.0f, my_dd = 0.0f;
-    int my_lim = 0;
+    uint64_t nl2 = 0ull, nd2 = 0ull;  // (-lse*log2e, -lse*log2e), (-D, -D)
+    int my_lim = 0;                   // keys [0, my_lim) are legal for this query
     if (!DKDV && own_row < p.n_q) {
-      my_lse2 = p.lse[(size_t)bh * p.n_q + own_row] * LOG2E;
-      my_dd = p.dd[(size_t)bh * p.n_q + own_row];
+      const float nl = -p.lse[(size_t)bh * p.n_q + own_row] * 1.4426950408889634f;
+      const float nd = -p.dd[(size_t)bh * p.n_q + own_row];
+      nl2 = ptx::f2_pack(nl, nl);
+      nd2 = ptx::f2_pack(nd, nd);
       my_lim = key_limit(own_row, kv_len, causal);
     }
+    const bool row_dead = DKDV ? own_row >= kv_len : my_lim == 0;
     bool ok = true;
     for (int u = 0; u < n_s && ok; ++u) {
       const int st = u % STAGES;
@@ -315,57 +330,62 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (DKDV && ok) ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_FULL + st), (u / STAGES) & 1, abort_flag));
       if (!ok) break;
       ptx::tc_fence_after();
-      const int s0 = (s_begin + u) * T;  // first streamed row (query for DKDV, key for dQ)
-      // four 32-column chunks: load S (X) and dP (Y), write P / dS as bf16 pairs into the
-      // columns already consumed
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      const int s0 = (s_begin + u) * T + g * 64;  // streamed row of this thread's first column
+      // columns [lo, hi) are legal for this thread; the rest get P = 0
+      int lo = 0, hi = 64;
+      if (DKDV) {
+        if (row_dead) hi = 0;
+        else if (causal) lo = max(0, own_row - s0);  // query >= key
+      } else {
+        hi = max(0, min(64, my_lim - s0));
+      }
+      const bool full = (lo == 0 && hi == 64);
+      const float* vnl = vec + st * T + g * 64;              // -lse*log2e of the columns (DKDV)
+      const float* vnd = vec + (STAGES + st) * T + g * 64;   // -D of the columns (DKDV)
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t xs[32], ys[32];
-        ptx::tmem_ld32(tmem + lane_off + C::TM_X + ch * 32, xs);
-        ptx::tmem_ld32(tmem + lane_off + C::TM_Y + ch * 32, ys);
+        ptx::tmem_ld32(t_x + ch * 32, xs);
+        ptx::tmem_ld32(t_y + ch * 32, ys);
         ptx::tmem_wait_ld();
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
-          float pp[2], dsv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = ch * 32 + x + e;
-            bool legal;
-            float lse2, dd;
-            if (DKDV) {  // own key own_row, query s0 + col
-              const int qi = s0 + col;
-              legal = own_row < kv_len && (!causal || qi >= own_row);
-              lse2 = vec[st * T + col] * LOG2E;
-              dd = vec[(STAGES + st) * T + col];
-            } else {     // own query own_row, key s0 + col
-              legal = s0 + col < my_lim;
-              lse2 = my_lse2;
-              dd = my_dd;
-            }
-            const float pv = legal ? ptx::ex2(fmaf(__uint_as_float(xs[x + e]), c, -lse2)) : 0.0f;
-            pp[e] = pv;
-            dsv[e] = pv * (__uint_as_float(ys[x + e]) - dd);
+          const int cc = ch * 32 + x;  // column within this warpgroup's half
+          uint64_t nl, nd;
+          if (DKDV) {
+            nl = *reinterpret_cast<const uint64_t*>(vnl + cc);
+            nd = *reinterpret_cast<const uint64_t*>(vnd + cc);
+          } else {
+            nl = nl2;
+            nd = nd2;
           }
-          pw[x >> 1] = ptx::pack_bf16x2(pp[0], pp[1]);
-          dw[x >> 1] = ptx::pack_bf16x2(dsv[0], dsv[1]);
+          float a0, a1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(xs[x]), __uint_as_float(xs[x + 1])), c2, nl), a0, a1);
+          float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+          if (!full) {
+            p0 = (cc >= lo && cc < hi) ? p0 : 0.0f;
+            p1 = (cc + 1 >= lo && cc + 1 < hi) ? p1 : 0.0f;
+          }
+          const uint64_t pp = ptx::f2_pack(p0, p1);
+          const uint64_t dp = ptx::f2_add(ptx::f2_pack(__uint_as_float(ys[x]), __uint_as_float(ys[x + 1])), nd);
+          float d0, d1;
+          ptx::f2_unpack(ptx::f2_mul(pp, dp), d0, d1);
+          if (DKDV) pw[x >> 1] = ptx::pack_bf16x2(p0, p1);
+          dw[x >> 1] = ptx::pack_bf16x2(d0, d1);
         }
-        // P (dkdv) goes over X, dS over Y (dkdv) or over X (dQ)
+        // P^T over X and dS^T over Y (DKDV), or dS over X (dQ), at columns 16 ch of
+        // this warpgroup's half: already read (chunk ch covers columns 32 ch .. 32 ch + 31)
         if (DKDV) {
           asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-                       ::"r"(tmem + lane_off + C::TM_X + ch * 16), "r"(pw[0]), "r"(pw[1]), "r"(pw[2]), "r"(pw[3]), "r"(pw[4]),
+                       ::"r"(t_x + ch * 16), "r"(pw[0]), "r"(pw[1]), "r"(pw[2]), "r"(pw[3]), "r"(pw[4]),
                        "r"(pw[5]), "r"(pw[6]), "r"(pw[7]), "r"(pw[8]), "r"(pw[9]), "r"(pw[10]), "r"(pw[11]), "r"(pw[12]),
                        "r"(pw[13]), "r"(pw[14]), "r"(pw[15]) : "memory");
-          asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-                       ::"r"(tmem + lane_off + C::TM_Y + ch * 16), "r"(dw[0]), "r"(dw[1]), "r"(dw[2]), "r"(dw[3]), "r"(dw[4]),
-                       "r"(dw[5]), "r"(dw[6]), "r"(dw[7]), "r"(dw[8]), "r"(dw[9]), "r"(dw[10]), "r"(dw[11]), "r"(dw[12]),
-                       "r"(dw[13]), "r"(dw[14]), "r"(dw[15]) : "memory");
-        } else {
-          asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-                       ::"r"(tmem + lane_off + C::TM_X + ch * 16), "r"(dw[0]), "r"(dw[1]), "r"(dw[2]), "r"(dw[3]), "r"(dw[4]),
-                       "r"(dw[5]), "r"(dw[6]), "r"(dw[7]), "r"(dw[8]), "r"(dw[9]), "r"(dw[10]), "r"(dw[11]), "r"(dw[12]),
-                       "r"(dw[13]), "r"(dw[14]), "r"(dw[15]) : "memory");
         }
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                     ::"r"((DKDV ? t_y : t_x) + ch * 16), "r"(dw[0]), "r"(dw[1]), "r"(dw[2]), "r"(dw[3]), "r"(dw[4]),
+                     "r"(dw[5]), "r"(dw[6]), "r"(dw[7]), "r"(dw[8]), "r"(dw[9]), "r"(dw[10]), "r"(dw[11]), "r"(dw[12]),
+                     "r"(dw[13]), "r"(dw[14]), "r"(dw[15]) : "memory");
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -373,6 +393,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
+    // DKDV: warpgroup 0 writes dK = scale * acc0, warpgroup 1 dV = acc1.
+    // dQ: warpgroup g writes columns [g D/2, g D/2 + D/2) of dQ = scale * acc0.
+    // A tile with nothing to stream (all keys padding, or rows past the end) writes zeros.
     const int n_rows = DKDV ? p.n_k : p.n_q;
     const bool row_valid = own_row < n_rows;
     if (ok && n_s > 0) {
@@ -380,33 +403,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok) ptx::tc_fence_after();
     }
     if (ok) {
-      // DKDV: g0 = dK = scale * acc0, g1 = dV = acc1; dQ: g0 = dQ = scale * acc0.
-      // A tile with nothing to stream (all keys padding, or rows past the end) writes zeros.
+      uint16_t* gout = (DKDV && g == 1) ? p.g1 : p.g0;
+      const float mul = (DKDV && g == 1) ? 1.0f : p.scale;
+      const uint32_t col0 = DKDV ? (g == 0 ? C::TM_ACC0 : C::TM_ACC1) : C::TM_ACC0 + g * (D / 2);
+      constexpr int NCH = DKDV ? D / 32 : D / 64;  // 32-column chunks this thread writes
+      uint16_t* grow = gout + ((size_t)bh * n_rows + (size_t)(row_valid ? own_row : 0)) * D + (DKDV ? 0 : g * (D / 2));
 #pragma unroll
-      for (int which = 0; which < (DKDV ? 2 : 1); ++which) {
-        uint16_t* g = which == 0 ? p.g0 : p.g1;
-        const float mul = which == 0 ? p.scale : 1.0f;
-        const uint32_t col0 = which == 0 ? C::TM_ACC0 : C::TM_ACC1;
-        uint16_t* grow = g + ((size_t)bh * n_rows + (size_t)(row_valid ? own_row : 0)) * D;
+      for (int q4 = 0; q4 < NCH; ++q4) {
+        uint32_t o[32];
+        if (n_s > 0) {
+          ptx::tmem_ld32(tmem + lane_off + col0 + q4 * 32, o);
+          ptx::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint32_t o[32];
-          if (n_s > 0) {
-            ptx::tmem_ld32(tmem + lane_off + col0 + q4 * 32, o);
-            ptx::tmem_wait_ld();
-          } else {
+          for (int x = 0; x < 32; ++x) o[x] = 0u;
+        }
+        uint32_t w[16];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = 0u;
-          }
-          uint32_t w[16];
+        for (int x = 0; x < 16; ++x)
+          w[x] = ptx::pack_bf16x2(__uint_as_float(o[2 * x]) * mul, __uint_as_float(o[2 * x + 1]) * mul);
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(grow + q4 * 32);
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
-            w[x] = ptx::pack_bf16x2(__uint_as_float(o[2 * x]) * mul, __uint_as_float(o[2 * x + 1]) * mul);
-          if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(grow + q4 * 32);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-          }
+          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
         }
       }
     }
