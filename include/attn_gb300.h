@@ -166,8 +166,9 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* cache_lens, void* stream);
 
 /*
- * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs (one fp32 per
- * query row: D_i below). Returns 0 for an invalid shape.
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: two fp32 per
+ * query row (-lse_i log2(e) and -D_i below), padded to whole 128-row tiles. Returns 0
+ * for an invalid shape.
  */
 size_t attn_bwd_workspace_size(int B, int h, int n_q);
 

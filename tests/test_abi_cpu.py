@@ -120,7 +120,7 @@ def test_decode_workspace_and_argument_checks(L):
 
 def test_bwd_workspace_and_argument_checks(L):
     ws = attn.attn_bwd_workspace_size
-    assert ws(2, 3, 500) == 2 * 3 * 500 * 4
+    assert ws(2, 3, 500) == 2 * 3 * 4 * 2 * 128 * 4  # 500 rows -> 4 tiles of 128
     assert ws(0, 1, 1) == 0 and ws(1, 1, 0) == 0
     need = ws(2, 3, 500)
     f = L.attn_bwd

@@ -10,7 +10,9 @@
 // "training").
 //
 // Three kernels, no atomics:
-//   attn_bwd_dot_kernel   D_i = dO_i . O_i (fp32), one warp per row;
+//   attn_bwd_dot_kernel   D_i = dO_i . O_i (fp32), one warp per row, written with
+//                         -lse_i log2(e) into a per-tile table the other two kernels
+//                         read (the dK/dV kernel with one bulk copy per query tile);
 //   attn_bwd_dkdv_kernel  one CTA per 128-key tile of one (b, h); it streams the
 //                         query tiles that can see its keys (Q_i, dO_i by TMA;
 //                         lse_i, D_i by the producer warp), computes
@@ -43,8 +45,8 @@ __device__ unsigned int g_bwd_fault_word;  // fault record of the gradient kerne
 namespace {
 
 constexpr int T = 128;          // rows per tile (queries or keys)
-// warps 0-7 elementwise (two warpgroups, one per half of the streamed tile's 128
-// columns), warp 8 TMA producer, warp 9 MMA issuer
+// warps 0-7 elementwise (two warpgroups, one per half of every streamed tile: its
+// rows 0-63 and 64-127), warp 8 TMA producer, warp 9 MMA issuer
 constexpr int EW_THREADS = 256;
 constexpr int THREADS = EW_THREADS + 64;
 constexpr int WARP_LOAD = 8, WARP_MMA = 9;
@@ -66,31 +68,32 @@ struct BCfg {
   static constexpr int OFF_A1 = OFF_A0 + TILE_BYTES;        // V (dkdv) or dO (dq)
   static constexpr int OFF_R0 = OFF_A1 + TILE_BYTES;        // ring: Q_i (dkdv) or K_j (dq)
   static constexpr int OFF_R1 = OFF_R0 + STAGES * TILE_BYTES;  // ring: dO_i (dkdv) or V_j (dq)
-  static constexpr int OFF_VEC = OFF_R1 + STAGES * TILE_BYTES;  // float -lse*log2e[STAGES][T], -D[STAGES][T]
+  static constexpr int OFF_VEC = OFF_R1 + STAGES * TILE_BYTES;  // float [STAGES][-lse*log2e[T], -D[T]]
   static constexpr int OFF_BAR = OFF_VEC + 2 * STAGES * T * 4;
-  // barriers: a_full, full[S], empty[S], mm_full, p_full, acc_done, drain
+  // barriers: a_full, full[S], empty[S], mm_full[2 halves], p_full[2 halves], acc_done, drain
   static constexpr int B_AFULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_MMFULL = B_EMPTY + STAGES;
-  static constexpr int B_PFULL = B_MMFULL + 1, B_ACC = B_PFULL + 1, B_DRAIN = B_ACC + 1, NUM_BARS = B_DRAIN + 1;
+  static constexpr int B_PFULL = B_MMFULL + 2, B_ACC = B_PFULL + 2, B_DRAIN = B_ACC + 1, NUM_BARS = B_DRAIN + 1;
   static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_SLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
-  // TMEM: X [0,128) = S^T or S, Y [128,256) = dP^T or dP, acc0 [256, 256+D), acc1 [256+D, 256+2D).
-  // The bf16 pairs written back over X and Y (P^T / dS^T, or dS) sit in columns
-  // [0, 32) for streamed rows 0-63 and [64, 96) for rows 64-127 of their region: each
-  // elementwise warpgroup writes only over columns it has already read.
-  static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
-  static constexpr uint32_t IDESC_NN = ptx::idesc_bf16_f32(T, T, false);  // both operands K-major
+  // TMEM: per half h of the streamed tile, X_h = 128h + [0,64) holds S^T or S and
+  // Y_h = 128h + [64,128) dP^T or dP (64 streamed rows each); acc0 [256, 256+D),
+  // acc1 [256+D, 256+2D). The bf16 pairs written back (P^T / dS^T, or dS) take the
+  // first 32 columns of X_h / Y_h, which their warpgroup has already read.
+  static constexpr uint32_t TM_ACC0 = 256, TM_ACC1 = 256 + D;
+  __host__ __device__ static constexpr uint32_t tm_x(int h) { return 128u * h; }
+  __host__ __device__ static constexpr uint32_t tm_y(int h) { return 128u * h + 64u; }
+  static constexpr uint32_t IDESC_NN = ptx::idesc_bf16_f32(T, T / 2, false);  // both operands K-major
   static constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(T, D, true);  // B MN-major
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 struct BwdParams {
-  const float* lse;    // [BH][n_q], natural log
-  const float* dd;     // [BH][n_q]  D_i = dO_i . O_i
+  const float* stats;  // [BH][q_tiles][2][T]: -lse_i log2(e), then -D_i; rows past n_q hold -inf, 0
   uint16_t* g0;        // dkdv: dK [BH][n_k][D];  dq: dQ [BH][n_q][D]
   uint16_t* g1;        // dkdv: dV [BH][n_k][D]
   const int32_t* key_lens;
-  int H, n_q, n_k, mask_mode, BH, tiles;
+  int H, n_q, n_k, mask_mode, BH, tiles, q_tiles;
   float scale, scale_log2;
 };
 
@@ -116,16 +119,37 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) return;
 }
 
+// Contiguous global -> shared copy (both 16-byte aligned, bytes a multiple of 16),
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 
 // ------------------------------------------------------------------ D_i = dO_i . O_i
+// Row r of the padded table (bh, tile, i): -lse_i log2(e) and -D_i, D_i = dO_i . O_i;
+// rows past n_q get -inf (so P = 0) and 0.
 template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const uint16_t* out, const uint16_t* dout, float* dd,
-                                                           long long rows) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const uint16_t* out, const uint16_t* dout, const float* lse,
+                                                           float* stats, int n_q, int q_tiles, long long rows) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // bh * q_tiles * T + i
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const uint32_t* o = reinterpret_cast<const uint32_t*>(out + row * D);
-  const uint32_t* g = reinterpret_cast<const uint32_t*>(dout + row * D);
+  const long long bh = row / ((long long)q_tiles * T);
+  const int i = (int)(row - bh * q_tiles * T);
+  float* dst = stats + (bh * q_tiles + i / T) * 2 * T + (i % T);
+  if (i >= n_q) {
+    if (lane == 0) {
+      dst[0] = -INFINITY;
+      dst[T] = 0.0f;
+    }
+    return;
+  }
+  const long long src = bh * n_q + i;
+  const uint32_t* o = reinterpret_cast<const uint32_t*>(out + src * D);
+  const uint32_t* g = reinterpret_cast<const uint32_t*>(dout + src * D);
   float acc = 0.0f;
 #pragma unroll
   for (int x = lane; x < D / 2; x += 32) {
@@ -135,7 +159,10 @@ __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const uint16_t* out, 
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dd[row] = acc;
+  if (lane == 0) {
+    dst[0] = -lse[src] * 1.4426950408889634f;
+    dst[T] = -acc;
+  }
 }
 
 // Legal key range of query row i of batch b: keys [0, lim).
@@ -157,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto bar = [&](int x) -> uint32_t { return s_base + C::OFF_BAR + 8u * x; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
-  float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // lse[S][T] then dd[S][T]
+  float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [S][-lse log2(e)[T], -D[T]]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int bh = blockIdx.x % p.BH;
@@ -184,11 +211,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(C::B_AFULL), 1);
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(bar(C::B_FULL + s), DKDV ? 1 + 32 : 1);  // TMA bytes (+ the producer lanes' vector stores)
+      ptx::mbar_init(bar(C::B_FULL + s), 1);  // TMA bytes
       ptx::mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    ptx::mbar_init(bar(C::B_MMFULL), 1);
-    ptx::mbar_init(bar(C::B_PFULL), EW_THREADS);
+    for (int h = 0; h < 2; ++h) {
+      ptx::mbar_init(bar(C::B_MMFULL + h), 1);
+      ptx::mbar_init(bar(C::B_PFULL + h), EW_THREADS / 2);
+    }
     ptx::mbar_init(bar(C::B_ACC), 1);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -221,24 +250,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         const int r0 = (s_begin + u) * T;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+          ptx::mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES + (DKDV ? 2 * T * 4 : 0));
+          if (DKDV)  // -lse log2(e) and -D of the 128 queries of this tile
+            bulk_copy(s_base + C::OFF_VEC + st * 2 * T * 4, p.stats + ((size_t)bh * p.q_tiles + s_begin + u) * 2 * T,
+                      2 * T * 4, bar(C::B_FULL + st));
           for (int c = 0; c < C::CHUNKS; ++c) {
             ptx::tma_load_3d(s_base + C::OFF_R0 + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_r0, bar(C::B_FULL + st),
                              c * 64, r0, bh, 0);
             ptx::tma_load_3d(s_base + C::OFF_R1 + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_r1, bar(C::B_FULL + st),
                              c * 64, r0, bh, 0);
           }
-        }
-        if (DKDV) {
-          // -lse*log2e and -D of the 128 queries of this tile (rows past n_q get
-          // -inf, so their P is 0)
-          for (int x = lane; x < T; x += 32) {
-            const int i = r0 + x;
-            const bool in = i < p.n_q;
-            vec[st * T + x] = in ? -p.lse[(size_t)bh * p.n_q + i] * 1.4426950408889634f : -INFINITY;
-            vec[(STAGES + st) * T + x] = in ? -p.dd[(size_t)bh * p.n_q + i] : 0.0f;
-          }
-          ptx::mbar_arrive(bar(C::B_FULL + st));
         }
         issued = u + 1;
       }
@@ -250,48 +271,69 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp == WARP_MMA) {
     // ================================================================ MMA issuer
+    // Half h of streamed tile u: S_h(u) and dP_h(u) (64 streamed rows), then, once its
+    // warpgroup has stored P / dS, the accumulations. Order: acc_h(u-1), S/dP_h(u) for
+    // h = 0, 1, so that one half's MMAs run while the other half's warpgroup works.
     if (lane == 0 && n_s > 0) {
-      bool ok = wait_bar(bar(C::B_AFULL), 0, abort_flag);
       const uint32_t a0 = s_base + C::OFF_A0, a1 = s_base + C::OFF_A1;
-      for (int u = 0; u < n_s && ok; ++u) {
-        const int st = u % STAGES;
-        ok = wait_bar(bar(C::B_FULL + st), (u / STAGES) & 1, abort_flag);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint32_t r0 = s_base + C::OFF_R0 + st * C::TILE_BYTES, r1 = s_base + C::OFF_R1 + st * C::TILE_BYTES;
-        // X = A0 R0^T, Y = A1 R1^T (both operands K-major along d)
+      auto stage0 = [&](int u) { return s_base + C::OFF_R0 + (u % STAGES) * C::TILE_BYTES; };
+      auto stage1 = [&](int u) { return s_base + C::OFF_R1 + (u % STAGES) * C::TILE_BYTES; };
+      // X_h = A0 R0_h^T, Y_h = A1 R1_h^T (both operands K-major along d); rows 64h.. of
+      // a streamed slab start 64h * 128 bytes in
+      auto issue_sdp = [&](int u, int h) {
+        const uint32_t r0 = stage0(u) + h * (T / 2) * 128, r1 = stage1(u) + h * (T / 2) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          ptx::mma_ss(tmem + C::TM_X, ptx::sdesc_sw128(a0 + koff, 16, 1024), ptx::sdesc_sw128(r0 + koff, 16, 1024),
+          ptx::mma_ss(tmem + C::tm_x(h), ptx::sdesc_sw128(a0 + koff, 16, 1024), ptx::sdesc_sw128(r0 + koff, 16, 1024),
                       C::IDESC_NN, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          ptx::mma_ss(tmem + C::TM_Y, ptx::sdesc_sw128(a1 + koff, 16, 1024), ptx::sdesc_sw128(r1 + koff, 16, 1024),
+          ptx::mma_ss(tmem + C::tm_y(h), ptx::sdesc_sw128(a1 + koff, 16, 1024), ptx::sdesc_sw128(r1 + koff, 16, 1024),
                       C::IDESC_NN, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(C::B_MMFULL));
-        ok = wait_bar(bar(C::B_PFULL), u & 1, abort_flag);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        // DKDV: dV += P^T dO_i (P^T over X), dK += dS^T Q_i (dS^T over Y), B = R1 / R0 MN-major
-        // dQ:   dQ += dS K_j (dS over X), B = R0 MN-major
+        ptx::mma_commit(bar(C::B_MMFULL + h));
+      };
+      // DKDV: dV += P_h^T dO_h, dK += dS_h^T Q_h; dQ: dQ += dS_h K_h. The bf16 pairs of
+      // streamed rows 64h + 16kk .. + 15 sit at X_h / Y_h + 8kk; B rows are MN-major.
+      auto issue_acc = [&](int u, int h) {
+        const uint32_t r0 = stage0(u), r1 = stage1(u);
 #pragma unroll
-        for (int kk = 0; kk < T / 16; ++kk) {
-          const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // bf16 pairs of streamed rows 16kk..16kk+15
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t brow = (h * 4 + kk) * 2048;
+          const uint32_t accum = (u > 0 || h > 0 || kk > 0) ? 1u : 0u;
           if (DKDV) {
-            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::TM_X + a_col, ptx::sdesc_sw128(r1 + kk * 2048, C::CHUNK_BYTES, 1024),
-                        C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_Y + a_col, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
-                        C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::tm_x(h) + kk * 8,
+                        ptx::sdesc_sw128(r1 + brow, C::CHUNK_BYTES, 1024), C::IDESC_ACC, accum);
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_y(h) + kk * 8,
+                        ptx::sdesc_sw128(r0 + brow, C::CHUNK_BYTES, 1024), C::IDESC_ACC, accum);
           } else {
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::TM_X + a_col, ptx::sdesc_sw128(r0 + kk * 2048, C::CHUNK_BYTES, 1024),
-                        C::IDESC_ACC, (u > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_x(h) + kk * 8,
+                        ptx::sdesc_sw128(r0 + brow, C::CHUNK_BYTES, 1024), C::IDESC_ACC, accum);
           }
         }
-        ptx::mma_commit(bar(C::B_EMPTY + st));  // the stage's tiles are consumed once these complete
+      };
+      bool ok = wait_bar(bar(C::B_AFULL), 0, abort_flag) && wait_bar(bar(C::B_FULL), 0, abort_flag);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_sdp(0, 0);
+        issue_sdp(0, 1);
+      }
+      for (int u = 1; u <= n_s && ok; ++u) {
+        if (u < n_s) {
+          ok = wait_bar(bar(C::B_FULL + u % STAGES), (u / STAGES) & 1, abort_flag);
+          if (!ok) break;
+        }
+        for (int h = 0; h < 2 && ok; ++h) {
+          ok = wait_bar(bar(C::B_PFULL + h), (u - 1) & 1, abort_flag);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_acc(u - 1, h);
+          if (h == 1) ptx::mma_commit(bar(C::B_EMPTY + (u - 1) % STAGES));  // tile u-1's stage is consumed
+          if (u < n_s) issue_sdp(u, h);
+        }
       }
       if (ok) ptx::mma_commit(bar(C::B_ACC));
       if (!ok) {
@@ -302,21 +344,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ================================================================ elementwise warpgroups
-    // Thread = own row (key for DKDV, query for dQ) = TMEM lane; warpgroup g takes the
-    // streamed tile's columns [64g, 64g + 64). No element needs another: P and dS of
-    // one (key, query) pair use only that pair's S, dP and the query's lse and D.
+    // Thread = own row (key for DKDV, query for dQ) = TMEM lane; warpgroup g takes half
+    // g of every streamed tile (its rows 64g .. 64g + 63 = the columns of X_g, Y_g). No
+    // element needs another: P and dS of one (key, query) pair use only that pair's S,
+    // dP and the query's lse and D.
     const int g = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t t_x = tmem + lane_off + C::TM_X + g * 64, t_y = tmem + lane_off + C::TM_Y + g * 64;
+    const uint32_t t_x = tmem + lane_off + C::tm_x(g), t_y = tmem + lane_off + C::tm_y(g);
     const int own_row = own0 + r;
     const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     // dQ: this thread's query statistics
     uint64_t nl2 = 0ull, nd2 = 0ull;  // (-lse*log2e, -lse*log2e), (-D, -D)
     int my_lim = 0;                   // keys [0, my_lim) are legal for this query
     if (!DKDV && own_row < p.n_q) {
-      const float nl = -p.lse[(size_t)bh * p.n_q + own_row] * 1.4426950408889634f;
-      const float nd = -p.dd[(size_t)bh * p.n_q + own_row];
+      const float* srow = p.stats + ((size_t)bh * p.q_tiles + own) * 2 * T + r;
+      const float nl = srow[0];
+      const float nd = srow[T];
       nl2 = ptx::f2_pack(nl, nl);
       nd2 = ptx::f2_pack(nd, nd);
       my_lim = key_limit(own_row, kv_len, causal);
@@ -325,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int u = 0; u < n_s && ok; ++u) {
       const int st = u % STAGES;
-      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_MMFULL), u & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_MMFULL + g), u & 1, abort_flag));
       // the stage's lse / D vectors (DKDV): already complete, waited on for ordering
       if (DKDV && ok) ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_FULL + st), (u / STAGES) & 1, abort_flag));
       if (!ok) break;
@@ -340,8 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         hi = max(0, min(64, my_lim - s0));
       }
       const bool full = (lo == 0 && hi == 64);
-      const float* vnl = vec + st * T + g * 64;              // -lse*log2e of the columns (DKDV)
-      const float* vnd = vec + (STAGES + st) * T + g * 64;   // -D of the columns (DKDV)
+      const float* vnl = vec + st * 2 * T + g * 64;      // -lse*log2e of the columns (DKDV)
+      const float* vnd = vec + st * 2 * T + T + g * 64;  // -D of the columns (DKDV)
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t xs[32], ys[32];
@@ -374,8 +418,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (DKDV) pw[x >> 1] = ptx::pack_bf16x2(p0, p1);
           dw[x >> 1] = ptx::pack_bf16x2(d0, d1);
         }
-        // P^T over X and dS^T over Y (DKDV), or dS over X (dQ), at columns 16 ch of
-        // this warpgroup's half: already read (chunk ch covers columns 32 ch .. 32 ch + 31)
+        // P^T over X_g and dS^T over Y_g (DKDV), or dS over X_g (dQ), at columns 16 ch:
+        // already read (chunk ch covers columns 32 ch .. 32 ch + 31)
         if (DKDV) {
           asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
                        ::"r"(t_x + ch * 16), "r"(pw[0]), "r"(pw[1]), "r"(pw[2]), "r"(pw[3]), "r"(pw[4]),
@@ -389,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_PFULL));
+      ptx::mbar_arrive(bar(C::B_PFULL + g));
     }
 
     // ---------------------------------------------------------------- epilogue
@@ -464,20 +508,22 @@ int set_smem_attr() {
 }
 
 template <int D>
-int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* dd) {
+int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats) {
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv, mdo;
   if (encode(enc, &mq, a.q, D, a.n_q, BH) != CUDA_SUCCESS || encode(enc, &mk, a.k, D, a.n_k, BH) != CUDA_SUCCESS ||
       encode(enc, &mv, a.v, D, a.n_k, BH) != CUDA_SUCCESS || encode(enc, &mdo, a.dout, D, a.n_q, BH) != CUDA_SUCCESS)
     return ATTN_ERR_UNSUPPORTED;
   if (set_smem_attr<D, true>() != ATTN_OK || set_smem_attr<D, false>() != ATTN_OK) return ATTN_ERR_CUDA;
-  const long long rows = (long long)BH * a.n_q;
+  const int q_tiles = (a.n_q + T - 1) / T;
+  const long long rows = (long long)BH * q_tiles * T;
+  if ((rows + 7) / 8 > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   attn_bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, a.stream>>>(
-      static_cast<const uint16_t*>(a.out), static_cast<const uint16_t*>(a.dout), dd, rows);
+      static_cast<const uint16_t*>(a.out), static_cast<const uint16_t*>(a.dout), a.lse, stats, a.n_q, q_tiles, rows);
   if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   BwdParams p;
-  p.lse = a.lse;
-  p.dd = dd;
+  p.stats = stats;
+  p.q_tiles = q_tiles;
   p.key_lens = a.key_lens;
   p.H = a.H;
   p.n_q = a.n_q;
@@ -506,12 +552,13 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* dd) {
 
 }  // namespace
 
-size_t bwd_workspace_bytes(int B, int H, int n_q) { return (size_t)B * H * n_q * sizeof(float); }
+// per (b, h) and 128-row query tile: -lse log2(e) and -D of its rows, 2 x 128 floats
+size_t bwd_workspace_bytes(int B, int H, int n_q) { return (size_t)B * H * ((n_q + T - 1) / T) * 2 * T * sizeof(float); }
 
 int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace) {
-  float* dd = static_cast<float*>(workspace);
-  if (a.d == 64) return launch_bwd<64>(a, enc, dd);
-  if (a.d == 128) return launch_bwd<128>(a, enc, dd);
+  float* stats = static_cast<float*>(workspace);
+  if (a.d == 64) return launch_bwd<64>(a, enc, stats);
+  if (a.d == 128) return launch_bwd<128>(a, enc, stats);
   return ATTN_ERR_UNSUPPORTED;
 }
 
