@@ -275,43 +275,42 @@ __global__ void __launch_bounds__(THREADS, 1)
     // warpgroup has stored P / dS, the accumulations. Order: acc_h(u-1), S/dP_h(u) for
     // h = 0, 1, so that one half's MMAs run while the other half's warpgroup works.
     if (lane == 0 && n_s > 0) {
-      const uint32_t a0 = s_base + C::OFF_A0, a1 = s_base + C::OFF_A1;
-      auto stage0 = [&](int u) { return s_base + C::OFF_R0 + (u % STAGES) * C::TILE_BYTES; };
-      auto stage1 = [&](int u) { return s_base + C::OFF_R1 + (u % STAGES) * C::TILE_BYTES; };
+      // Shared-memory descriptors are built once and advanced by adding (offset >> 4)
+      // to the start-address field (addresses stay below 2^18, so the 14-bit field never
+      // carries): this thread issues every MMA of the CTA and is kept lean.
+      const uint64_t d_a0 = ptx::sdesc_sw128(s_base + C::OFF_A0, 16, 1024);
+      const uint64_t d_a1 = ptx::sdesc_sw128(s_base + C::OFF_A1, 16, 1024);
+      const uint64_t d_r0k = ptx::sdesc_sw128(s_base + C::OFF_R0, 16, 1024);              // K-major view
+      const uint64_t d_r1k = ptx::sdesc_sw128(s_base + C::OFF_R1, 16, 1024);
+      const uint64_t d_r0m = ptx::sdesc_sw128(s_base + C::OFF_R0, C::CHUNK_BYTES, 1024);  // MN-major view
+      const uint64_t d_r1m = ptx::sdesc_sw128(s_base + C::OFF_R1, C::CHUNK_BYTES, 1024);
+      auto koff16 = [](int kk) { return (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4); };
       // X_h = A0 R0_h^T, Y_h = A1 R1_h^T (both operands K-major along d); rows 64h.. of
       // a streamed slab start 64h * 128 bytes in
       auto issue_sdp = [&](int u, int h) {
-        const uint32_t r0 = stage0(u) + h * (T / 2) * 128, r1 = stage1(u) + h * (T / 2) * 128;
+        const uint64_t so = (uint64_t)(((u % STAGES) * C::TILE_BYTES + h * (T / 2) * 128) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          ptx::mma_ss(tmem + C::tm_x(h), ptx::sdesc_sw128(a0 + koff, 16, 1024), ptx::sdesc_sw128(r0 + koff, 16, 1024),
-                      C::IDESC_NN, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + C::tm_x(h), d_a0 + koff16(kk), d_r0k + so + koff16(kk), C::IDESC_NN, kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          ptx::mma_ss(tmem + C::tm_y(h), ptx::sdesc_sw128(a1 + koff, 16, 1024), ptx::sdesc_sw128(r1 + koff, 16, 1024),
-                      C::IDESC_NN, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_ss(tmem + C::tm_y(h), d_a1 + koff16(kk), d_r1k + so + koff16(kk), C::IDESC_NN, kk > 0 ? 1u : 0u);
         ptx::mma_commit(bar(C::B_MMFULL + h));
       };
       // DKDV: dV += P_h^T dO_h, dK += dS_h^T Q_h; dQ: dQ += dS_h K_h. The bf16 pairs of
       // streamed rows 64h + 16kk .. + 15 sit at X_h / Y_h + 8kk; B rows are MN-major.
       auto issue_acc = [&](int u, int h) {
-        const uint32_t r0 = stage0(u), r1 = stage1(u);
+        const uint64_t so = (uint64_t)(((u % STAGES) * C::TILE_BYTES) >> 4);
+        const uint32_t first = (u > 0 || h > 0) ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t brow = (h * 4 + kk) * 2048;
-          const uint32_t accum = (u > 0 || h > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t brow = (uint64_t)(((h * 4 + kk) * 2048) >> 4);
+          const uint32_t accum = kk > 0 ? 1u : first;
           if (DKDV) {
-            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::tm_x(h) + kk * 8,
-                        ptx::sdesc_sw128(r1 + brow, C::CHUNK_BYTES, 1024), C::IDESC_ACC, accum);
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_y(h) + kk * 8,
-                        ptx::sdesc_sw128(r0 + brow, C::CHUNK_BYTES, 1024), C::IDESC_ACC, accum);
+            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::tm_x(h) + kk * 8, d_r1m + so + brow, C::IDESC_ACC, accum);
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_y(h) + kk * 8, d_r0m + so + brow, C::IDESC_ACC, accum);
           } else {
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_x(h) + kk * 8,
-                        ptx::sdesc_sw128(r0 + brow, C::CHUNK_BYTES, 1024), C::IDESC_ACC, accum);
+            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_x(h) + kk * 8, d_r0m + so + brow, C::IDESC_ACC, accum);
           }
         }
       };
