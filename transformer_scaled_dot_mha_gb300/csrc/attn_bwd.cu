@@ -46,9 +46,10 @@ namespace {
 
 constexpr int T = 128;          // rows per tile (queries or keys)
 // warps 0-7 elementwise (two warpgroups, one per half of every streamed tile: its
-// rows 0-63 and 64-127), warp 8 TMA producer, warp 9 MMA issuer
+// rows 0-63 and 64-127), warp 8 TMA producer, warps 9 and 10 MMA issuers (one per
+// half; warp 9 serves both halves where the two halves' accumulators do not fit TMEM)
 constexpr int EW_THREADS = 256;
-constexpr int THREADS = EW_THREADS + 64;
+constexpr int THREADS = EW_THREADS + 96;
 constexpr int WARP_LOAD = 8, WARP_MMA = 9;
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -70,17 +71,16 @@ struct BCfg {
   static constexpr int OFF_R1 = OFF_R0 + STAGES * TILE_BYTES;  // ring: dO_i (dkdv) or V_j (dq)
   static constexpr int OFF_VEC = OFF_R1 + STAGES * TILE_BYTES;  // float [STAGES][-lse*log2e[T], -D[T]]
   static constexpr int OFF_BAR = OFF_VEC + 2 * STAGES * T * 4;
-  // barriers: a_full, full[S], empty[S], mm_full[2 halves], p_full[2 halves], acc_done, drain
+  // barriers: a_full, full[S], empty[S], mm_full[2 halves], p_full[2 halves], acc_done, drain[2 issuers]
   static constexpr int B_AFULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_MMFULL = B_EMPTY + STAGES;
-  static constexpr int B_PFULL = B_MMFULL + 2, B_ACC = B_PFULL + 2, B_DRAIN = B_ACC + 1, NUM_BARS = B_DRAIN + 1;
+  static constexpr int B_PFULL = B_MMFULL + 2, B_ACC = B_PFULL + 2, B_DRAIN = B_ACC + 1, NUM_BARS = B_DRAIN + 2;
   static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_SLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
   // TMEM: per half h of the streamed tile, X_h = 128h + [0,64) holds S^T or S and
-  // Y_h = 128h + [64,128) dP^T or dP (64 streamed rows each); acc0 [256, 256+D),
-  // acc1 [256+D, 256+2D). The bf16 pairs written back (P^T / dS^T, or dS) take the
+  // Y_h = 128h + [64,128) dP^T or dP (64 streamed rows each); the accumulators follow
+  // from column 256 (acc_col). The bf16 pairs written back (P^T / dS^T, or dS) take the
   // first 32 columns of X_h / Y_h, which their warpgroup has already read.
-  static constexpr uint32_t TM_ACC0 = 256, TM_ACC1 = 256 + D;
   __host__ __device__ static constexpr uint32_t tm_x(int h) { return 128u * h; }
   __host__ __device__ static constexpr uint32_t tm_y(int h) { return 128u * h + 64u; }
   static constexpr uint32_t IDESC_NN = ptx::idesc_bf16_f32(T, T / 2, false);  // both operands K-major
@@ -178,6 +178,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                        const BwdParams p) {
   using C = BCfg<D>;
   constexpr int STAGES = C::STAGES;
+  // One issuer per half, each with its own accumulators (summed in the epilogue): for
+  // the dQ kernel at D = 128, where the two halves' MMAs outrun one issuing thread
+  // (same-box A/B: +3 %; at D = 64, and for dK/dV, one issuer measured as fast or
+  // faster, and two dK/dV issuers would not fit TMEM at D = 128).
+  constexpr bool SPLIT = !DKDV && D == 128;
+  // TMEM column of accumulator `which` (DKDV: 0 = dK, 1 = dV; dQ: 0) of half h
+  auto acc_col = [](int which, int h) -> uint32_t {
+    if (!DKDV) return 256u + (SPLIT ? h : 0) * D;
+    return SPLIT ? 256u + h * 128u + which * 64u : 256u + which * D;
+  };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = ptx::smem_u32(smem);
@@ -212,14 +222,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::mbar_init(bar(C::B_AFULL), 1);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(bar(C::B_FULL + s), 1);  // TMA bytes
-      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
+      ptx::mbar_init(bar(C::B_EMPTY + s), SPLIT ? 2 : 1);  // one commit per issuer
     }
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(bar(C::B_MMFULL + h), 1);
       ptx::mbar_init(bar(C::B_PFULL + h), EW_THREADS / 2);
     }
-    ptx::mbar_init(bar(C::B_ACC), 1);
+    ptx::mbar_init(bar(C::B_ACC), SPLIT ? 2 : 1);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
+    ptx::mbar_init(bar(C::B_DRAIN + 1), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -269,12 +280,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int u = max(0, issued - STAGES); u < issued; ++u) drain_wait(bar(C::B_FULL + u % STAGES), (u / STAGES) & 1);
     }
     __syncwarp();
-  } else if (warp == WARP_MMA) {
-    // ================================================================ MMA issuer
+  } else if (warp >= WARP_MMA) {
+    // ================================================================ MMA issuers
     // Half h of streamed tile u: S_h(u) and dP_h(u) (64 streamed rows), then, once its
-    // warpgroup has stored P / dS, the accumulations. Order: acc_h(u-1), S/dP_h(u) for
-    // h = 0, 1, so that one half's MMAs run while the other half's warpgroup works.
-    if (lane == 0 && n_s > 0) {
+    // warpgroup has stored P / dS, the accumulations. SPLIT: warp WARP_MMA + h serves
+    // half h. Otherwise warp WARP_MMA serves both, in the order acc_h(u-1), S/dP_h(u)
+    // for h = 0, 1, and warp WARP_MMA + 1 idles.
+    if (lane == 0 && n_s > 0 && (SPLIT || warp == WARP_MMA)) {
       // Shared-memory descriptors are built once and advanced by adding (offset >> 4)
       // to the start-address field (addresses stay below 2^18, so the 14-bit field never
       // carries): this thread issues every MMA of the CTA and is kept lean.
@@ -301,20 +313,40 @@ __global__ void __launch_bounds__(THREADS, 1)
       // streamed rows 64h + 16kk .. + 15 sit at X_h / Y_h + 8kk; B rows are MN-major.
       auto issue_acc = [&](int u, int h) {
         const uint64_t so = (uint64_t)(((u % STAGES) * C::TILE_BYTES) >> 4);
-        const uint32_t first = (u > 0 || h > 0) ? 1u : 0u;
+        const uint32_t first = (u > 0 || (!SPLIT && h > 0)) ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t brow = (uint64_t)(((h * 4 + kk) * 2048) >> 4);
           const uint32_t accum = kk > 0 ? 1u : first;
           if (DKDV) {
-            ptx::mma_ts(tmem + C::TM_ACC1, tmem + C::tm_x(h) + kk * 8, d_r1m + so + brow, C::IDESC_ACC, accum);
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_y(h) + kk * 8, d_r0m + so + brow, C::IDESC_ACC, accum);
+            ptx::mma_ts(tmem + acc_col(1, h), tmem + C::tm_x(h) + kk * 8, d_r1m + so + brow, C::IDESC_ACC, accum);
+            ptx::mma_ts(tmem + acc_col(0, h), tmem + C::tm_y(h) + kk * 8, d_r0m + so + brow, C::IDESC_ACC, accum);
           } else {
-            ptx::mma_ts(tmem + C::TM_ACC0, tmem + C::tm_x(h) + kk * 8, d_r0m + so + brow, C::IDESC_ACC, accum);
+            ptx::mma_ts(tmem + acc_col(0, h), tmem + C::tm_x(h) + kk * 8, d_r0m + so + brow, C::IDESC_ACC, accum);
           }
         }
       };
       bool ok = wait_bar(bar(C::B_AFULL), 0, abort_flag) && wait_bar(bar(C::B_FULL), 0, abort_flag);
+      if (SPLIT) {
+        // this warp serves half hs only: acc_hs(u-1), then S/dP_hs(u)
+        const int hs = warp - WARP_MMA;
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_sdp(0, hs);
+        }
+        for (int u = 1; u <= n_s && ok; ++u) {
+          if (u < n_s) {
+            ok = wait_bar(bar(C::B_FULL + u % STAGES), (u / STAGES) & 1, abort_flag);
+            if (!ok) break;
+          }
+          ok = wait_bar(bar(C::B_PFULL + hs), (u - 1) & 1, abort_flag);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_acc(u - 1, hs);
+          ptx::mma_commit(bar(C::B_EMPTY + (u - 1) % STAGES));  // this half of tile u-1 is consumed
+          if (u < n_s) issue_sdp(u, hs);
+        }
+      } else {
       if (ok) {
         ptx::tc_fence_after();
         issue_sdp(0, 0);
@@ -334,15 +366,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (u < n_s) issue_sdp(u, h);
         }
       }
+      }
       if (ok) ptx::mma_commit(bar(C::B_ACC));
       if (!ok) {
-        ptx::mma_commit(bar(C::B_DRAIN));
-        drain_wait(bar(C::B_DRAIN), 0);
+        ptx::mma_commit(bar(C::B_DRAIN + (warp - WARP_MMA)));
+        drain_wait(bar(C::B_DRAIN + (warp - WARP_MMA)), 0);
       }
     }
     __syncwarp();
   } else {
-    // ================================================================ elementwise warpgroups
+    // ================================================================ elementwise warpgroups (warps 0-7)
     // Thread = own row (key for DKDV, query for dQ) = TMEM lane; warpgroup g takes half
     // g of every streamed tile (its rows 64g .. 64g + 63 = the columns of X_g, Y_g). No
     // element needs another: P and dS of one (key, query) pair use only that pair's S,
@@ -436,8 +469,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    // DKDV: warpgroup 0 writes dK = scale * acc0, warpgroup 1 dV = acc1.
-    // dQ: warpgroup g writes columns [g D/2, g D/2 + D/2) of dQ = scale * acc0.
+    // DKDV: warpgroup 0 writes dK = scale * (its accumulators), warpgroup 1 dV.
+    // dQ: warpgroup g writes columns [g D/2, g D/2 + D/2) of dQ = scale * accumulator.
+    // With one issuer per half (SPLIT) each result is the sum of the halves' accumulators.
     // A tile with nothing to stream (all keys padding, or rows past the end) writes zeros.
     const int n_rows = DKDV ? p.n_k : p.n_q;
     const bool row_valid = own_row < n_rows;
@@ -448,7 +482,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok) {
       uint16_t* gout = (DKDV && g == 1) ? p.g1 : p.g0;
       const float mul = (DKDV && g == 1) ? 1.0f : p.scale;
-      const uint32_t col0 = DKDV ? (g == 0 ? C::TM_ACC0 : C::TM_ACC1) : C::TM_ACC0 + g * (D / 2);
+      const uint32_t col0 = DKDV ? acc_col(g, 0) : acc_col(0, 0) + g * (D / 2);
+      const uint32_t col1 = DKDV ? acc_col(g, 1) : acc_col(0, 1) + g * (D / 2);  // the other half's (SPLIT)
       constexpr int NCH = DKDV ? D / 32 : D / 64;  // 32-column chunks this thread writes
       uint16_t* grow = gout + ((size_t)bh * n_rows + (size_t)(row_valid ? own_row : 0)) * D + (DKDV ? 0 : g * (D / 2));
 #pragma unroll
@@ -456,7 +491,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t o[32];
         if (n_s > 0) {
           ptx::tmem_ld32(tmem + lane_off + col0 + q4 * 32, o);
-          ptx::tmem_wait_ld();
+          if (SPLIT) {
+            uint32_t o1[32];
+            ptx::tmem_ld32(tmem + lane_off + col1 + q4 * 32, o1);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) + __uint_as_float(o1[x]));
+          } else {
+            ptx::tmem_wait_ld();
+          }
         } else {
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = 0u;
