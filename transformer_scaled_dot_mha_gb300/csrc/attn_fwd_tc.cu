@@ -56,8 +56,6 @@ namespace {
 
 constexpr int BM = 128;  // query rows per Q tile (= TMEM lanes)
 constexpr int BN = 128;  // keys per K/V tile
-constexpr int WARP_LOAD = 8;
-constexpr int WARP_MMA0 = 9;  // MMA issuer of Q tile 0; WARP_MMA0 + 1 issues for Q tile 1
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain copies in flight
@@ -65,14 +63,21 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when ma
 
 constexpr uint32_t FAULT_PRODUCER = 1, FAULT_MMA = 2, FAULT_SOFTMAX = 4, FAULT_EPILOGUE = 8;
 
-template <int D>
+// SINGLE (D = 64, short sequences): one 128-row Q tile per CTA, 256 TMEM columns, a
+// two-stage ring and 8 warps, so that two CTAs share an SM; used when the two-tile
+// grid would not fill two waves of the GPU. Otherwise two Q tiles per CTA.
+template <int D, bool SINGLE = false>
 struct Cfg {
+  static_assert(!SINGLE || D == 64, "single-tile variant is for d = 64");
+  static constexpr int Q_TILES = SINGLE ? 1 : 2;  // Q tiles per CTA
+  static constexpr int ROWS = Q_TILES * BM;       // query rows per CTA
+  static constexpr int CTAS_PER_SM = SINGLE ? 2 : 1;
   static constexpr int CHUNKS = D / 64;           // 128-byte swizzle atoms per row
   static constexpr int CHUNK_BYTES = BM * 128;    // one 128-row x 64-column slab
   static constexpr int TILE_BYTES = BM * D * 2;   // one 128-row tile of Q, K or V
-  static constexpr int STAGES = (D == 64) ? 4 : 2;
+  static constexpr int STAGES = SINGLE ? 2 : (D == 64) ? 4 : 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_K = OFF_Q + Q_TILES * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
   // barrier indices
@@ -91,22 +96,29 @@ struct Cfg {
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TMEM_COLS = SINGLE ? 256 : 512;
   static constexpr bool SEP_P = (D == 64);  // P has its own TMEM columns
-  // SEP_P: four MMA issuers (S and PV per Q tile) -> 16 warps; else one issuer, 12 warps.
-  // Register split (setmaxnreg): control warps give registers to the softmax warps;
-  // the total stays equal to the launch allocation.
-  static constexpr int THREADS = SEP_P ? 512 : 384;
+  // Warps: the softmax warpgroups (one per Q tile), the TMA producer, then the MMA
+  // issuers -- with SEP_P four roles (S and PV per Q tile, roles 0-1 and 2-3), else one.
+  // SEP_P: 16 warps (8 with SINGLE, where roles 0-2 exist and role 1 has no tile);
+  // else 12. Register split (setmaxnreg): control warps give registers to the softmax
+  // warps; the total stays equal to the launch allocation.
+  static constexpr int SOFTMAX_WARPS = 4 * Q_TILES;
+  static constexpr int SOFTMAX_THREADS = 32 * SOFTMAX_WARPS;
+  static constexpr int WARP_LOAD = SOFTMAX_WARPS;
+  static constexpr int WARP_MMA0 = SOFTMAX_WARPS + 1;  // MMA issuer role 0 (S of Q tile 0)
+  static constexpr int THREADS = SINGLE ? 256 : SEP_P ? 512 : 384;
   static constexpr int REGS_CONTROL = SEP_P ? 40 : 56;
   static constexpr int REGS_SOFTMAX = SEP_P ? 216 : 224;
-  static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;  // 128 or 168 per thread
-  static_assert((THREADS - 256) * REGS_CONTROL + 256 * REGS_SOFTMAX == THREADS * LAUNCH_REGS, "register split");
-  static constexpr uint32_t TMEM_P = SEP_P ? 2 * BN : 0;          // + t * (SEP_P ? 64 : BN)
+  static constexpr int LAUNCH_REGS = (65536 / (THREADS * CTAS_PER_SM)) & ~7;  // 128 or 168 per thread
+  static_assert((THREADS - SOFTMAX_THREADS) * REGS_CONTROL + SOFTMAX_THREADS * REGS_SOFTMAX == THREADS * LAUNCH_REGS,
+                "register split");
+  static constexpr uint32_t TMEM_P = SINGLE ? BN : SEP_P ? 2 * BN : 0;    // + t * (SEP_P ? 64 : BN)
   static constexpr uint32_t TMEM_P_STRIDE = SEP_P ? BN / 2 : BN;
-  static constexpr uint32_t TMEM_O = SEP_P ? 3 * BN : 2 * BN;     // + t * D
+  static constexpr uint32_t TMEM_O = SINGLE ? BN + BN / 2 : SEP_P ? 3 * BN : 2 * BN;  // + t * D
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);  // Q, K both K-major
   static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);   // V is MN-major
-  static_assert(TMEM_O + 2 * D <= TMEM_COLS, "TMEM budget");
+  static_assert(TMEM_O + Q_TILES * D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -182,11 +194,11 @@ __device__ __forceinline__ uint16_t* out_row_of(const Params& p, int b, int bh, 
 // HEADS_INTERLEAVED: Q, K, V and out are [B, n, h*d] (the projections' own layout,
 // before split_heads / after the concatenation of the heads) instead of [B, h, n, d];
 // the tensor maps then span (h*d, n, B) and a head is an x offset of h*d.
-template <int D, bool LOCAL, bool HEADS_INTERLEAVED>
-__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+template <int D, bool LOCAL, bool HEADS_INTERLEAVED, bool SINGLE>
+__global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_PER_SM)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, SINGLE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = ptx::smem_u32(smem);
@@ -198,13 +210,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- which 256 query rows of which (b, h): heaviest causal blocks first
+  // ---- which C::ROWS query rows of which (b, h): heaviest causal blocks first
   const int bh = blockIdx.x % p.BH;
   const int qb = p.num_qblocks - 1 - blockIdx.x / p.BH;
   const int b = bh / p.H;
   const int tma_z = HEADS_INTERLEAVED ? b : bh;                   // TMA z coordinate of this head
   const int tma_x = HEADS_INTERLEAVED ? (bh - b * p.H) * D : 0;  // and its x offset
-  const int row0 = qb * 2 * BM;
+  const int row0 = qb * C::ROWS;
   const bool causal = (p.mask_mode & 1) != 0;
   int kv_len = p.n_k;
   if (p.mask_mode & 2) kv_len = min(max(p.key_lens[b], 0), p.n_k);
@@ -216,7 +228,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   } else {
     const int kv_tiles = (kv_len + BN - 1) / BN;
     n_t0 = tiles_for(row0, p.n_q, kv_tiles, causal);
-    n_t1 = tiles_for(row0 + BM, p.n_q, kv_tiles, causal);
+    n_t1 = SINGLE ? 0 : tiles_for(row0 + BM, p.n_q, kv_tiles, causal);
   }
   // the K/V ring carries tiles J0 .. J0 + n_max - 1 (ring use u holds tile J0 + u);
   // tile 1 starts no earlier than tile 0, and tile 0 has work whenever tile 1 has
@@ -243,11 +255,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == WARP_MMA0) {
+  if (warp == C::WARP_MMA0) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
-  if (warp == WARP_LOAD && lane == 0) {
+  if (warp == C::WARP_LOAD && lane == 0) {
     ptx::prefetch_tmap(&tm_q);
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
@@ -257,9 +269,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 8) {
+  if (warp >= C::SOFTMAX_WARPS) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CONTROL));
-    if (warp == WARP_LOAD) {
+    if (warp == C::WARP_LOAD) {
     // ================================================================ producer
     if (lane == 0 && n_max > 0) {
       const uint64_t pol_q = ptx::policy_evict_first();
@@ -303,10 +315,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
     }
     __syncwarp();
-    } else if (warp >= WARP_MMA0 && warp < WARP_MMA0 + 4) {
+    } else if (warp >= C::WARP_MMA0 && warp < C::WARP_MMA0 + 4) {
     // ================================================================ MMA issuers
     // SEP_P: warp 9 + t issues S_t, warp 11 + t issues PV_t. Otherwise warp 9 issues all.
-    const int role = warp - WARP_MMA0;
+    const int role = warp - C::WARP_MMA0;
     const int t = role & 1;  // Q tile
     const int n_t = t ? n_t1 : n_t0;
     const int n_o = t ? n_t0 : n_t1;  // tiles of the other Q tile
@@ -638,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   // ---- teardown
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == WARP_MMA0) {
+  if (warp == C::WARP_MMA0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -667,15 +679,16 @@ CUresult encode_map_interleaved(PFN_encodeTiled enc, CUtensorMap* map, const voi
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D, bool LOCAL, bool HEADS_INTERLEAVED>
+template <int D, bool LOCAL, bool HEADS_INTERLEAVED, bool SINGLE = false>
 int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv) {
-  using C = Cfg<D>;
+  using C = Cfg<D, SINGLE>;
   // the shared-memory opt-in is per device; set it once for each device used
   static std::atomic<bool> attr_done[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_done[dev].store(true, std::memory_order_release);
@@ -690,13 +703,28 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
   p.mask_mode = a.mask_mode;
   p.window = a.window;
   p.BH = a.B * a.H;
-  p.num_qblocks = (a.n_q + 2 * BM - 1) / (2 * BM);
+  p.num_qblocks = (a.n_q + C::ROWS - 1) / C::ROWS;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   const long long grid = (long long)p.BH * p.num_qblocks;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv,
-                                                                                                         p);
+  attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(
+      mq, mk, mv, p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Short sequences: when the two-tile grid would not fill two waves of the GPU, one Q
+// tile per CTA and two CTAs per SM keep more SMs busy and overlap their latencies.
+bool use_single_tile(const TcArgs& a) {
+  static std::atomic<int> sm_count[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  int n = sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return false;
+    sm_count[dev].store(n, std::memory_order_relaxed);
+  }
+  const long long two_tile_grid = (long long)a.B * a.H * ((a.n_q + 2 * BM - 1) / (2 * BM));
+  return two_tile_grid < 2LL * n;
 }
 
 template <int D>
@@ -708,13 +736,16 @@ int launch(const TcArgs& a, PFN_encodeTiled enc) {
         encode_map_interleaved(enc, &mk, a.k, D, a.H, a.n_k, a.B) != CUDA_SUCCESS ||
         encode_map_interleaved(enc, &mv, a.v, D, a.H, a.n_k, a.B) != CUDA_SUCCESS)
       return ATTN_ERR_UNSUPPORTED;
+    if (D == 64 && use_single_tile(a)) return launch_variant<D, false, true, D == 64>(a, mq, mk, mv);
     return launch_variant<D, false, true>(a, mq, mk, mv);
   }
   if (encode_map(enc, &mq, a.q, D, a.n_q, a.B * a.H) != CUDA_SUCCESS ||
       encode_map(enc, &mk, a.k, D, a.n_k, a.B * a.H) != CUDA_SUCCESS ||
       encode_map(enc, &mv, a.v, D, a.n_k, a.B * a.H) != CUDA_SUCCESS)
     return ATTN_ERR_UNSUPPORTED;
-  return a.window >= 0 ? launch_variant<D, true, false>(a, mq, mk, mv) : launch_variant<D, false, false>(a, mq, mk, mv);
+  if (a.window >= 0) return launch_variant<D, true, false>(a, mq, mk, mv);
+  if (D == 64 && use_single_tile(a)) return launch_variant<D, false, false, D == 64>(a, mq, mk, mv);
+  return launch_variant<D, false, false>(a, mq, mk, mv);
 }
 
 }  // namespace
