@@ -524,7 +524,12 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
 
       // mask: key-length boundary, the causal diagonal, the local window
       const int j0 = (jb + j) * BN;
-      const bool edge = (j0 + BN > kv_len) || (causal && j0 + BN - 1 > row0 + t * BM) || windowed;
+      // a tile needs the mask unless every key is legal for every row of the Q tile: the
+      // window test asks whether keys [j0, j0 + BN) lie within [i - window, i + window]
+      // for all rows i of [r0, r0 + BM)
+      const int r0t = row0 + t * BM;
+      const bool edge = (j0 + BN > kv_len) || (causal && j0 + BN - 1 > r0t) ||
+                        (windowed && (j0 < r0t + BM - 1 - window || j0 + BN - 1 > r0t + window));
       if (edge) {
         int lim = kv_len - j0;  // columns [first, lim) are legal
         if (causal) lim = min(lim, i - j0 + 1);
