@@ -80,6 +80,39 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
              int mask_mode, const int32_t* key_lens, void* stream);
 
 /*
+ * attn_fwd_host_workspace_size -- bytes of device workspace attn_fwd_host needs for
+ * this shape and mask (four chunk slots of Q, K, V, out, lse plus the key lengths;
+ * the mask enters through the chunk plan). Returns 0 for an invalid shape or mask
+ * (d must be 64 or 128). Depends only on the arguments.
+ */
+size_t attn_fwd_host_workspace_size(int B, int h, int n_q, int n_k, int d, int mask_mode);
+
+/*
+ * attn_fwd_host -- attn_fwd for operands that live in HOST memory, the call an
+ * application makes when its Q, K, V are not yet on the GPU. Same operation, masks,
+ * numerics and results as attn_fwd (bit for bit: the same kernel runs on each chunk).
+ *   q, k, v, key_lens: host memory, read by the call;   out, lse: host memory, written.
+ *   Page-locked (pinned) host memory is strongly recommended: with pageable memory the
+ *   copies are staged by the driver and do not overlap the kernels.
+ *   workspace: device scratch of at least attn_fwd_host_workspace_size(B, h, n_q,
+ *   n_k, d_k, mask_mode) bytes, 256-byte aligned, owned by the caller.
+ * The flattened (b, h) head range is cut into chunks. Chunk c's host-to-device copy,
+ * its attention kernel and its device-to-host copy run on the library's own streams
+ * (one for each direction, one per slot for the kernels) through a four-slot ring in
+ * the workspace, so transfers overlap computation and consecutive kernels overlap
+ * each other. Every stream waits for what `stream` had queued before the call, and
+ * `stream` waits for all of them. The call is asynchronous: the host buffers must
+ * stay valid and unmodified (q, k, v, key_lens) or unread (out, lse) until `stream`
+ * reaches this call's end, which includes every copy back; calls made
+ * from several host threads are serialised per device. Errors as attn_fwd; a failure
+ * after some chunks were queued returns ATTN_ERR_CUDA with those chunks in flight.
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse,
+                  int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
+                  int mask_mode, const int32_t* key_lens, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
  * attn_fwd_local -- restricted (local-window) self-attention, bf16, on the same
  * tensor-core kernel as attn_fwd. The pages propose, for very long sequences,
  * letting each position attend only to positions within a neighbourhood r, which

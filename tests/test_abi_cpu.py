@@ -141,3 +141,40 @@ def test_bwd_workspace_and_argument_checks(L):
     assert call(d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED
     assert call(d_v=128) == attn.ATTN_ERR_UNSUPPORTED
     assert call(scale=float("inf")) == attn.ATTN_ERR_INVALID
+
+
+def test_host_forward_workspace_and_argument_checks(L):
+    ws = attn.attn_fwd_host_workspace_size
+    # 32 heads of 28160 input bytes: under the 8 MiB minimum chunk, so one chunk and one
+    # slot of q 32*100*64*2, k and v 32*60*64*2, out as q, lse 32*100*4 (each 256-byte
+    # aligned), after 16 key lengths padded to 256 bytes
+    assert ws(16, 2, 100, 60, 64) == 256 + 409600 + 2 * 245760 + 409600 + 12800
+    # 32 heads of n = 8192, 3 MiB of input each (minimum chunk 3 heads). Per head q, k,
+    # v, out are 1 MiB each and lse 32 KiB.
+    per_head = 4 * 8192 * 64 * 2 + 8192 * 4
+    # no mask: a head's kernel (~17 us at 1 PFLOP/s) is over 0.6 of its copies (~21 us
+    # at 200 GB/s), so eight equal chunks of 4 heads; four slots of 4 heads
+    assert ws(2, 16, 8192, 8192, 64) == 256 + 16 * per_head
+    # causal: half the kernel time, transfer-bound, so the ramp 3, 6, 12, 6, 5; the four
+    # slots hold chunks {3, 5}, {6}, {12}, {6}
+    assert ws(2, 16, 8192, 8192, 64, 1) == 256 + (5 + 6 + 12 + 6) * per_head
+    assert ws(1, 1, 8, 8, 64, 4) == 0
+    assert ws(1, 1, 1, 1, 96) == 0 and ws(0, 1, 1, 1, 64) == 0 and ws(1, 1, 1, 0, 64) == 0
+    need = ws(2, 3, 500, 500, 64, 1)
+    ok = dict(q=16, k=32, v=48, out=64, lse=None, B=2, h=3, n_q=500, n_k=500, d_k=64, d_v=64, scale=0.125,
+              mask=1, lens=None, ws=256, nbytes=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.attn_fwd_host(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["h"], a["n_q"], a["n_k"],
+                               a["d_k"], a["d_v"], a["scale"], a["mask"], a["lens"], a["ws"], a["nbytes"], None)
+    assert call(nbytes=need - 1) == attn.ATTN_ERR_INVALID      # workspace too small
+    assert call(ws=None) == attn.ATTN_ERR_INVALID
+    assert call(ws=272) == attn.ATTN_ERR_INVALID               # workspace not 256-byte aligned
+    for name in ("q", "k", "v", "out"):
+        assert call(**{name: None}) == attn.ATTN_ERR_INVALID
+    assert call(n_k=400) == attn.ATTN_ERR_INVALID              # causal needs n_q == n_k
+    assert call(mask=2) == attn.ATTN_ERR_INVALID               # key padding without key_lens
+    assert call(d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(d_v=128) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID

@@ -38,6 +38,10 @@ def lib() -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
         L.attn_fwd.restype = i
+        L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.attn_fwd_host_workspace_size.restype = ctypes.c_size_t
+        L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, ctypes.c_size_t, vp]
+        L.attn_fwd_host.restype = i
         L.attn_fwd_local.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
         L.attn_fwd_local.restype = i
         L.attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
@@ -111,6 +115,39 @@ def _call(fn, q, k, v, out, lse, scale, mask_mode, key_lens, stream, dtype, wher
 def attn_fwd(q, k, v, out, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
     """bf16 forward into caller-provided ``out`` (and optional fp32 ``lse``)."""
     return _call(lib().attn_fwd, q, k, v, out, lse, scale, mask_mode, key_lens, stream, torch.bfloat16, "attn_fwd")
+
+
+def attn_fwd_host_workspace_size(B, H, n_q, n_k, d, mask_mode=MASK_NONE) -> int:
+    return int(lib().attn_fwd_host_workspace_size(B, H, n_q, n_k, d, int(mask_mode)))
+
+
+def attn_fwd_host(q, k, v, out, workspace, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
+    """bf16 forward on HOST tensors (pinned recommended): q, k, v, key_lens are read
+    and out, lse written in host memory; the chunked copy/compute pipeline runs on
+    the GPU with ``workspace`` (a CUDA uint8 tensor of attn_fwd_host_workspace_size
+    bytes) and is asynchronous on ``stream``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous 4-D host bf16 tensor, got {t.dtype} {tuple(t.shape)}")
+    B, H, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    if k.shape != (B, H, n_k, d_k) or v.shape != (B, H, n_k, d_v) or out.shape != (B, H, n_q, d_v):
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)} out{tuple(out.shape)}")
+    if lse is not None and (lse.dtype != torch.float32 or lse.is_cuda or not lse.is_contiguous()
+                            or lse.shape != (B, H, n_q)):
+        raise ValueError("lse must be a contiguous host float32 tensor of shape [B, H, n_q]")
+    if key_lens is not None and (key_lens.dtype != torch.int32 or key_lens.is_cuda or key_lens.shape != (B,)):
+        raise ValueError("key_lens must be a host int32 tensor of shape [B]")
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    st = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, n_q, n_k, d_k, d_v,
+                             float(scale), int(mask_mode), _ptr(key_lens), _ptr(workspace), workspace.numel(),
+                             _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_host")
+    return out
 
 
 def attn_fwd_local(q, k, v, out, window, lse=None, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):

@@ -61,6 +61,29 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   return attn::launch_attn_tc(a, enc);
 }
 
+size_t attn_fwd_host_workspace_size(int B, int h, int n_q, int n_k, int d, int mask_mode) {
+  if (B <= 0 || h <= 0 || n_q <= 0 || n_k <= 0 || (d != 64 && d != 128)) return 0;
+  if (mask_mode < 0 || mask_mode > (ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return 0;
+  const long long bh = (long long)B * h;
+  if (bh > 0x7fffffffLL || bh * (n_q > n_k ? n_q : n_k) > (1LL << 40) / d) return 0;
+  return attn::host_workspace_bytes(B, h, n_q, n_k, d, mask_mode);
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse, int B, int h, int n_q,
+                  int n_k, int d_k, int d_v, float scale, int mask_mode, const int32_t* key_lens, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  int st = check_common(q, k, v, out, lse, B, h, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (!workspace || !aligned(workspace, 256)) return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < attn::host_workspace_bytes(B, h, n_q, n_k, d_k, mask_mode)) return ATTN_ERR_INVALID;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::TcArgs a{q, k, v, out, lse, B, h, n_q, n_k, d_k, scale, mask_mode, key_lens,
+                 static_cast<cudaStream_t>(stream), -1};
+  return attn::launch_attn_host(a, enc, workspace);
+}
+
 int attn_fwd_local(const void* q, const void* k, const void* v, void* out, float* lse, int B, int h, int n,
                    int d_k, int d_v, float scale, int window, int mask_mode, const int32_t* key_lens,
                    void* stream) {

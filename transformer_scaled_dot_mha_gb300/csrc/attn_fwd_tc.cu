@@ -719,7 +719,10 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
 
 // Short sequences: when the two-tile grid would not fill two waves of the GPU, one Q
 // tile per CTA and two CTAs per SM keep more SMs busy and overlap their latencies.
+}  // namespace
+
 bool use_single_tile(const TcArgs& a) {
+  if (a.single_tile >= 0) return a.single_tile == 1 && a.d == 64 && a.window < 0;
   static std::atomic<int> sm_count[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -731,6 +734,8 @@ bool use_single_tile(const TcArgs& a) {
   const long long two_tile_grid = (long long)a.B * a.H * ((a.n_q + 2 * BM - 1) / (2 * BM));
   return two_tile_grid < 2LL * n;
 }
+
+namespace {
 
 template <int D>
 int launch(const TcArgs& a, PFN_encodeTiled enc) {
