@@ -60,7 +60,7 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "a15b97a6954f4d7e"): 142595584,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "4146bd9c4867a47d"): 142052608,
     # profiles/attn_decode_split_kernel_decode_b16_h16_q1_k8192_d64.md (split kernel only)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_split_kernel", "72652789c3570524"): 424460032,
 }
