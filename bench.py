@@ -462,7 +462,7 @@ def run_ours_grad(args, w):
     lse = torch.empty((w.B, w.H, w.n_q), dtype=torch.float32, device=dev)
     attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws = torch.empty(attn.attn_bwd_workspace_size(w.B, w.H, w.n_q), dtype=torch.uint8, device=dev)
+    ws = torch.empty(attn.attn_bwd_workspace_size(w.B, w.H, w.n_q, w.d_k), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 

@@ -63,6 +63,9 @@ typedef enum {
 
 enum { ATTN_MASK_NONE = 0, ATTN_MASK_CAUSAL = 1, ATTN_MASK_KEY_PADDING = 2 };
 
+/* attn_bwd flags */
+enum { ATTN_BWD_DETERMINISTIC = 1 };
+
 /*
  * attn_fwd -- bf16 inputs and output, fp32 accumulation (sm_103a tensor cores).
  *   q, k, v, out: bf16 (raw 16-bit) arrays, 16-byte aligned.
@@ -199,11 +202,13 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* cache_lens, void* stream);
 
 /*
- * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: two fp32 per
- * query row (-lse_i log2(e) and -D_i below), padded to whole 128-row tiles. Returns 0
- * for an invalid shape.
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs for this shape,
+ * head size d and flags: two fp32 per query row (-lse_i log2(e) and -D_i below),
+ * padded to whole 128-row tiles, plus, for the fused schedule (d = 64 without
+ * ATTN_BWD_DETERMINISTIC), an fp32 dQ accumulator of B*h*n_q*64 floats. Returns 0 for
+ * an invalid shape, head size or flag.
  */
-size_t attn_bwd_workspace_size(int B, int h, int n_q);
+size_t attn_bwd_workspace_size(int B, int h, int n_q, int d, int flags);
 
 /*
  * attn_bwd -- gradients of attn_fwd with respect to q, k and v, given the gradient
@@ -218,19 +223,28 @@ size_t attn_bwd_workspace_size(int B, int h, int n_q);
  *           for the same q, k, v, scale, mask_mode and key_lens; lse is required)
  *   dq [B, h, n_q, d], dk, dv [B, h, n_k, d]: bf16, written in full (a key that no
  *           query may see gets dk = dv = 0; a query with no legal key gets dq = 0)
- *   workspace: device scratch of at least attn_bwd_workspace_size(B, h, n_q) bytes,
- *           16-byte aligned, owned by the caller, contents undefined on return;
- *           concurrent calls must not share it.
+ *   flags: 0, or ATTN_BWD_DETERMINISTIC (any other bit: ATTN_ERR_INVALID).
+ *   workspace: device scratch of at least attn_bwd_workspace_size(B, h, n_q, d_k,
+ *           flags) bytes, 16-byte aligned, owned by the caller, contents undefined on
+ *           return; concurrent calls must not share it.
  * mask_mode and key_lens as in attn_fwd. Supported: d_k == d_v in {64, 128}.
  * Numerics: S and dP accumulate in fp32 on the tensor cores; P and dS are rounded to
  * bf16 before the three products that consume them, which accumulate in fp32; D_i
  * is accumulated in fp32 from the bf16 out and dout; results are rounded to bf16
- * once. Three kernels are launched on `stream`, no atomics: the results are
- * deterministic.
+ * once. Schedules:
+ *   - fused (d = 64, flags = 0): each of the five products is computed once; the
+ *     partial dQ of every 128-key tile is added into the fp32 workspace accumulator
+ *     with TMA reduce-adds, whose order varies, so the last bits of dq can differ
+ *     from run to run (dk and dv are deterministic). A memset and three kernels.
+ *   - deterministic (d = 128, or ATTN_BWD_DETERMINISTIC): a dK/dV kernel and a dQ
+ *     kernel that recomputes S and dP (seven products), no atomics: bit-identical
+ *     results on every run. Three kernels.
+ * All launches are on `stream`.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
-             int mask_mode, const int32_t* key_lens, void* workspace, size_t workspace_bytes, void* stream);
+             int mask_mode, const int32_t* key_lens, int flags, void* workspace, size_t workspace_bytes,
+             void* stream);
 
 /*
  * attn_mha_workspace_size -- bytes of device workspace attn_mha_fwd needs: the

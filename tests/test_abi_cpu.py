@@ -120,18 +120,20 @@ def test_decode_workspace_and_argument_checks(L):
 
 def test_bwd_workspace_and_argument_checks(L):
     ws = attn.attn_bwd_workspace_size
-    assert ws(2, 3, 500) == 2 * 3 * 4 * 2 * 128 * 4  # 500 rows -> 4 tiles of 128
-    assert ws(0, 1, 1) == 0 and ws(1, 1, 0) == 0
-    need = ws(2, 3, 500)
+    stats = 2 * 3 * 4 * 2 * 128 * 4  # 500 rows -> 4 tiles of 128, two floats per row
+    assert ws(2, 3, 500, 64, attn.BWD_DETERMINISTIC) == stats and ws(2, 3, 500, 128, 0) == stats
+    assert ws(2, 3, 500, 64, 0) == stats + 2 * 3 * 500 * 64 * 4  # + the fused schedule's fp32 dQ
+    assert ws(0, 1, 1) == 0 and ws(1, 1, 0) == 0 and ws(1, 1, 8, 96) == 0 and ws(1, 1, 8, 64, 2) == 0
+    need = ws(2, 3, 500, 64, 0)
     f = L.attn_bwd
     ok = dict(q=16, k=32, v=48, out=64, dout=80, lse=96, dq=112, dk=128, dv=144, B=2, h=3, n_q=500, n_k=500,
-              d_k=64, d_v=64, scale=0.125, mask=1, lens=None, ws=160, nbytes=need)
+              d_k=64, d_v=64, scale=0.125, mask=1, lens=None, flags=0, ws=160, nbytes=need)
 
     def call(**kw):
         a = dict(ok, **kw)
         return f(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"], a["h"],
-                 a["n_q"], a["n_k"], a["d_k"], a["d_v"], a["scale"], a["mask"], a["lens"], a["ws"], a["nbytes"],
-                 None)
+                 a["n_q"], a["n_k"], a["d_k"], a["d_v"], a["scale"], a["mask"], a["lens"], a["flags"], a["ws"],
+                 a["nbytes"], None)
     assert call(nbytes=need - 1) == attn.ATTN_ERR_INVALID      # workspace too small
     for name in ("dout", "lse", "dq", "dk", "dv", "ws"):
         assert call(**{name: None}) == attn.ATTN_ERR_INVALID
@@ -141,6 +143,9 @@ def test_bwd_workspace_and_argument_checks(L):
     assert call(d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED
     assert call(d_v=128) == attn.ATTN_ERR_UNSUPPORTED
     assert call(scale=float("inf")) == attn.ATTN_ERR_INVALID
+    assert call(flags=2) == attn.ATTN_ERR_INVALID              # unknown flag
+    # the deterministic schedule's workspace is too small for the fused one (d = 64, flags 0)
+    assert call(nbytes=ws(2, 3, 500, 64, attn.BWD_DETERMINISTIC)) == attn.ATTN_ERR_INVALID
 
 
 def test_host_forward_workspace_and_argument_checks(L):

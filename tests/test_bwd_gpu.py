@@ -20,7 +20,9 @@ by at most u of the value), |.| element-wise:
     |lse|) together) P is off by rP_ij P_ij, rP_ij = scale g (|Q||K|^T)_ij + that;
     so dS also carries x_ij = P_ij eP_ij + rP_ij P_ij |dP_ij - D_i|;
   * dV, dK and dQ accumulate n_q, n_q and n_k products in fp32 (a = n 2^-23 of
-    their sums of absolute values) and are rounded to bf16 once (u |g|).
+    their sums of absolute values) and are rounded to bf16 once (u |g|). The fused
+    schedule (d = 64) forms dQ from 128-key partial sums added in fp32 in memory:
+    fewer than n_k additions, so the same allowance covers it.
 Worst case per element (all rounding errors aligned), checked as |err| <= 1.25
 bound (the quarter covers the neglected second-order products of these terms):
   bound(dV) = (u + rP + a_q) P^T|dout| + u|dV|
@@ -72,16 +74,16 @@ def draw(seed, B, H, n_q, n_k, d, mask, lens=None):
     return q, k, v, dout, np.asarray(lens, np.int32)
 
 
-def run_bwd(q, k, v, dout, scale, mask, lens):
+def run_bwd(q, k, v, dout, scale, mask, lens, flags=0):
     B, H, n_q, d = q.shape
     qd, kd, vd, gd = dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_bf16(dout)
     kl = torch.from_numpy(lens).cuda() if mask & W.MASK_KEY_PADDING else None
     out = torch.empty_like(qd)
     lse = torch.empty((B, H, n_q), dtype=torch.float32, device="cuda")
     attn.attn_fwd(qd, kd, vd, out, lse, scale, mask, kl)
-    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, n_q), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, n_q, d, flags), dtype=torch.uint8, device="cuda")
     dq, dk, dv = torch.full_like(qd, float("nan")), torch.full_like(kd, float("nan")), torch.full_like(vd, float("nan"))
-    attn.attn_bwd(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, scale, mask, kl)
+    attn.attn_bwd(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, scale, mask, kl, flags=flags)
     torch.cuda.synchronize()
     f = lambda t: t.float().cpu().numpy().astype(np.float64)
     return (f(dq), f(dk), f(dv)), f(out)
@@ -139,10 +141,10 @@ def check(got, ref, bnd):
             f"{name}: ||err|| {np.linalg.norm(err):.3e} above the quadrature bound {np.linalg.norm(qb):.3e}")
 
 
-def parity(orc, seed, B, H, n_q, n_k, d, mask, lens=None, scale=None):
+def parity(orc, seed, B, H, n_q, n_k, d, mask, lens=None, scale=None, flags=0):
     q, k, v, dout, lens = draw(seed, B, H, n_q, n_k, d, mask, lens)
     scale = W.default_scale(d) if scale is None else scale
-    got, out_dev = run_bwd(q, k, v, dout, scale, mask, lens)
+    got, out_dev = run_bwd(q, k, v, dout, scale, mask, lens, flags)
     kl = lens if mask & W.MASK_KEY_PADDING else None
     ref = orc.attention_bwd(q, k, v, dout, scale, mask, kl)
     bnd = bounds(orc, q, k, v, dout, scale, mask, kl, ref, out_dev)
@@ -151,11 +153,11 @@ def parity(orc, seed, B, H, n_q, n_k, d, mask, lens=None, scale=None):
     return got, ref
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d,flags", [(64, 0), (64, attn.BWD_DETERMINISTIC), (128, 0)])
 @pytest.mark.parametrize("mask", [W.MASK_NONE, W.MASK_CAUSAL])
 @pytest.mark.parametrize("n", [1, 64, 128, 300, 513])
-def test_bwd_self(orc, d, mask, n):
-    parity(orc, 7000 + d + n + 3 * mask, 2, 2, n, n, d, mask)
+def test_bwd_self(orc, d, flags, mask, n):
+    parity(orc, 7000 + d + n + 3 * mask, 2, 2, n, n, d, mask, flags=flags)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -185,13 +187,29 @@ def test_bwd_dead_keys_get_zero_gradient(orc):
     assert np.all(dk[1] == 0) and np.all(dv[1] == 0) and np.all(dq[1] == 0)
 
 
-def test_bwd_deterministic():
-    """No atomics: two calls give bit-identical gradients."""
-    q, k, v, dout, lens = draw(7500, 2, 4, 700, 700, 64, W.MASK_CAUSAL)
-    a, _ = run_bwd(q, k, v, dout, W.default_scale(64), W.MASK_CAUSAL, lens)
-    b, _ = run_bwd(q, k, v, dout, W.default_scale(64), W.MASK_CAUSAL, lens)
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_deterministic(d):
+    """The deterministic schedule (no atomics): two calls give bit-identical gradients."""
+    q, k, v, dout, lens = draw(7500, 2, 4, 700, 700, d, W.MASK_CAUSAL)
+    a, _ = run_bwd(q, k, v, dout, W.default_scale(d), W.MASK_CAUSAL, lens, attn.BWD_DETERMINISTIC)
+    b, _ = run_bwd(q, k, v, dout, W.default_scale(d), W.MASK_CAUSAL, lens, attn.BWD_DETERMINISTIC)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("mask", [W.MASK_CAUSAL, W.MASK_KEY_PADDING])
+def test_bwd_fused_matches_deterministic(orc, mask):
+    """The fused schedule (d = 64) runs the dK and dV products in the same order as the
+    deterministic one, so dk and dv agree bit for bit; dq (reduced in memory, in varying
+    order) must meet the derived bounds (checked by parity) and stay within a few bf16
+    ulps of the deterministic dq."""
+    q, k, v, dout, lens = draw(7550 + mask, 3, 2, 700, 700, 64, mask, lens=[700, 333, 1])
+    fused, _ = run_bwd(q, k, v, dout, W.default_scale(64), mask, lens, 0)
+    det, _ = run_bwd(q, k, v, dout, W.default_scale(64), mask, lens, attn.BWD_DETERMINISTIC)
+    assert np.array_equal(fused[1], det[1]) and np.array_equal(fused[2], det[2])
+    diff = np.abs(fused[0] - det[0])
+    assert np.all(diff <= 4 * U * np.abs(det[0]) + 1e-6), f"dq differs by up to {diff.max():.3e}"
+    parity(orc, 7550 + mask, 3, 2, 700, 700, 64, mask, lens=[700, 333, 1])
 
 
 @pytest.mark.parametrize("d,mask", [(64, W.MASK_CAUSAL), (128, W.MASK_NONE)])
@@ -213,7 +231,7 @@ def test_bwd_rejects_small_workspace():
     q, k, v, dout, lens = draw(7700, 1, 1, 64, 64, 64, W.MASK_NONE)
     qd, kd, vd, gd = dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_bf16(dout)
     lse = torch.zeros((1, 1, 64), dtype=torch.float32, device="cuda")
-    ws = torch.empty(attn.attn_bwd_workspace_size(1, 1, 64) - 16, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(attn.attn_bwd_workspace_size(1, 1, 64, 64) - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(attn.AttnError) as e:
         attn.attn_bwd(qd, kd, vd, qd, gd, lse, torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd), ws)
     assert e.value.status == attn.ATTN_ERR_INVALID

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gb3
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 0, -1, -2, -3, -4
 MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+BWD_DETERMINISTIC = 1  # attn_bwd flag: the two-kernel schedule, bit-identical on every run
 
 _lib = None
 
@@ -52,10 +53,10 @@ def lib() -> ctypes.CDLL:
         L.attn_decode.restype = i
         L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
         L.attn_decode_noalloc.restype = i
-        L.attn_bwd_workspace_size.argtypes = [i, i, i]
+        L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
         L.attn_bwd_workspace_size.restype = ctypes.c_size_t
-        L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, ctypes.c_size_t,
-                               vp]
+        L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp,
+                               ctypes.c_size_t, vp]
         L.attn_bwd.restype = i
         L.attn_mha_workspace_size.argtypes = [i, i, i, i, i, i]
         L.attn_mha_workspace_size.restype = ctypes.c_size_t
@@ -244,15 +245,16 @@ def attn_decode_noalloc(q, k_cache, v_cache, out, cache_lens, lse=None, scale=No
     return out
 
 
-def attn_bwd_workspace_size(B, H, n_q) -> int:
-    return int(lib().attn_bwd_workspace_size(B, H, n_q))
+def attn_bwd_workspace_size(B, H, n_q, d=64, flags=0) -> int:
+    return int(lib().attn_bwd_workspace_size(B, H, n_q, d, int(flags)))
 
 
 def attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, scale=None, mask_mode=MASK_NONE, key_lens=None,
-             stream=None):
+             stream=None, flags=0):
     """Gradients of attn_fwd into caller-provided ``dq``, ``dk``, ``dv`` (bf16, shaped like
     q, k, v), given ``dout`` and the forward's ``out`` and fp32 ``lse``; ``workspace`` is a
-    CUDA tensor of at least ``attn_bwd_workspace_size`` bytes."""
+    CUDA tensor of at least ``attn_bwd_workspace_size(B, H, n_q, d, flags)`` bytes;
+    ``flags`` = BWD_DETERMINISTIC selects the bit-reproducible schedule."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, torch.bfloat16)
     B, H, n_q, d_k = q.shape
@@ -273,8 +275,8 @@ def attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, scale=None, mask_mo
         scale = 1.0 / math.sqrt(d_k)
     nbytes = workspace.numel() * workspace.element_size()
     st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                        B, H, n_q, n_k, d_k, d_v, float(scale), int(mask_mode), _ptr(key_lens), _ptr(workspace),
-                        nbytes, _stream_handle(stream))
+                        B, H, n_q, n_k, d_k, d_v, float(scale), int(mask_mode), _ptr(key_lens), int(flags),
+                        _ptr(workspace), nbytes, _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv

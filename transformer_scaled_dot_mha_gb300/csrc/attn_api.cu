@@ -148,26 +148,30 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
   return attn::launch_attn_decode_noalloc(a);
 }
 
-size_t attn_bwd_workspace_size(int B, int h, int n_q) {
+size_t attn_bwd_workspace_size(int B, int h, int n_q, int d, int flags) {
   if (B <= 0 || h <= 0 || n_q <= 0 || (long long)B * h > 0x7fffffffLL) return 0;
-  return attn::bwd_workspace_bytes(B, h, n_q);
+  if ((d != 64 && d != 128) || (flags & ~ATTN_BWD_DETERMINISTIC)) return 0;
+  if ((long long)B * h * n_q > (1LL << 40) / 64) return 0;
+  return attn::bwd_workspace_bytes(B, h, n_q, d, flags);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
-             int mask_mode, const int32_t* key_lens, void* workspace, size_t workspace_bytes, void* stream) {
+             int mask_mode, const int32_t* key_lens, int flags, void* workspace, size_t workspace_bytes,
+             void* stream) {
   int st = check_common(q, k, v, out, lse, B, h, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens);
   if (st != ATTN_OK) return st;
   if (!dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID;
+  if (flags & ~ATTN_BWD_DETERMINISTIC) return ATTN_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 16))
     return ATTN_ERR_INVALID;
   if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
-  if (workspace_bytes < attn::bwd_workspace_bytes(B, h, n_q)) return ATTN_ERR_INVALID;
+  if (workspace_bytes < attn::bwd_workspace_bytes(B, h, n_q, d_k, flags)) return ATTN_ERR_INVALID;
   attn::PFN_encodeTiled enc = tensor_map_encoder();
   if (!enc) return ATTN_ERR_CUDA;
   attn::BwdArgs a{q, k, v, out, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, mask_mode, key_lens,
-                  static_cast<cudaStream_t>(stream)};
+                  static_cast<cudaStream_t>(stream), flags};
   return attn::launch_attn_bwd(a, enc, workspace);
 }
 

@@ -9,7 +9,8 @@
 // (training the model needs them: attention-paper-guide section 05; vlmlib.cn
 // "training").
 //
-// Three kernels, no atomics:
+// Two schedules. The deterministic one (any d, or on request) has three kernels and
+// no atomics:
 //   attn_bwd_dot_kernel   D_i = dO_i . O_i (fp32), one warp per row, written with
 //                         -lse_i log2(e) into a per-tile table the other two kernels
 //                         read (the dK/dV kernel with one bulk copy per query tile);
@@ -23,6 +24,13 @@
 //   attn_bwd_dq_kernel    one CTA per 128-query tile; it streams the key tiles,
 //                         computes S = Q K_j^T and dP = dO V_j^T, forms dS (thread =
 //                         query) and accumulates dQ += dS K_j.
+// The fused one (d = 64) computes each product once: the dK/dV kernel also writes
+// dS^T to shared memory and forms the partial dQ_i = dS_i K (one more MMA per
+// streamed tile, into one of two TMEM buffers); four drain warps move each partial
+// through shared memory into an fp32 accumulator in global memory with TMA
+// reduce-adds, and attn_bwd_dq_convert_kernel scales and rounds it to bf16. Five
+// products instead of seven; the order of the reduce-adds, and so the last bits of
+// dQ, varies from run to run.
 // Every operand layout is one the forward kernel already uses: a [rows][d] tile
 // loaded with 128-byte swizzling is a K-major operand along d and an MN-major
 // operand along d. Waits are bounded as in the forward kernel; a wait that runs
@@ -31,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -49,18 +58,25 @@ constexpr int T = 128;          // rows per tile (queries or keys)
 // rows 0-63 and 64-127), warp 8 TMA producer, warps 9 and 10 MMA issuers (one per
 // half; warp 9 serves both halves where the two halves' accumulators do not fit TMEM)
 constexpr int EW_THREADS = 256;
-constexpr int THREADS = EW_THREADS + 96;
 constexpr int WARP_LOAD = 8, WARP_MMA = 9;
+constexpr int WARP_DRAIN = 12;  // fused: warps 12-15 drain the dQ partials (warp 11 idles)
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t FAULT_BWD = 32;
 
-template <int D>
+template <int D, bool FUSED = false>
 struct BCfg {
+  static_assert(!FUSED || D == 64, "the fused schedule is for d = 64");
+  static constexpr int THREADS = FUSED ? 512 : EW_THREADS + 96;
+  // fused: setmaxnreg split of the 512 x 128 launch registers
+  static constexpr int REGS_EW = 176, REGS_CTRL = 80;
+  static_assert(!FUSED || EW_THREADS * REGS_EW + (THREADS - EW_THREADS) * REGS_CTRL == THREADS * (65536 / THREADS),
+                "register split");
   // ring depth; with d = 64 the deeper ring also keeps a second CTA (which would
-  // block on the 512-column TMEM allocation) off the SM
-  static constexpr int STAGES = D == 64 ? 4 : 2;
+  // block on the 512-column TMEM allocation) off the SM; the fused schedule gives
+  // one stage to the dS and dQ staging tiles
+  static constexpr int STAGES = FUSED ? 3 : D == 64 ? 4 : 2;
   static constexpr int CHUNKS = D / 64;
   static constexpr int CHUNK_BYTES = T * 128;
   static constexpr int TILE_BYTES = T * D * 2;
@@ -70,10 +86,17 @@ struct BCfg {
   static constexpr int OFF_R0 = OFF_A1 + TILE_BYTES;        // ring: Q_i (dkdv) or K_j (dq)
   static constexpr int OFF_R1 = OFF_R0 + STAGES * TILE_BYTES;  // ring: dO_i (dkdv) or V_j (dq)
   static constexpr int OFF_VEC = OFF_R1 + STAGES * TILE_BYTES;  // float [STAGES][-lse*log2e[T], -D[T]]
-  static constexpr int OFF_BAR = OFF_VEC + 2 * STAGES * T * 4;
-  // barriers: a_full, full[S], empty[S], mm_full[2 halves], p_full[2 halves], acc_done, drain[2 issuers]
+  // fused: dS^T of the streamed tile, [2 query halves][T keys][128 B] (128-byte
+  // swizzle; the MN-major A operand of dQ_i = dS_i K), then the fp32 dQ staging tiles,
+  // [4 row quarters][2 column halves][32 rows][128 B] (128-byte swizzle, the reduce's box)
+  static constexpr int OFF_DS = (OFF_VEC + 2 * STAGES * T * 4 + 1023) & ~1023;
+  static constexpr int OFF_DQS = OFF_DS + (FUSED ? 2 * CHUNK_BYTES : 0);
+  static constexpr int OFF_BAR = OFF_DQS + (FUSED ? 2 * CHUNK_BYTES : 0);
+  // barriers: a_full, full[S], empty[S], mm_full[2 halves], p_full[2 halves], acc_done, drain[2 issuers],
+  // fused: dq_full[2 buffers] (partial computed), dq_free[2 buffers] (partial read out of TMEM)
   static constexpr int B_AFULL = 0, B_FULL = 1, B_EMPTY = B_FULL + STAGES, B_MMFULL = B_EMPTY + STAGES;
-  static constexpr int B_PFULL = B_MMFULL + 2, B_ACC = B_PFULL + 2, B_DRAIN = B_ACC + 1, NUM_BARS = B_DRAIN + 2;
+  static constexpr int B_PFULL = B_MMFULL + 2, B_ACC = B_PFULL + 2, B_DRAIN = B_ACC + 1;
+  static constexpr int B_DQFULL = B_DRAIN + 2, B_DQFREE = B_DQFULL + 2, NUM_BARS = B_DQFREE + 2;
   static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_SLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
@@ -85,6 +108,10 @@ struct BCfg {
   __host__ __device__ static constexpr uint32_t tm_y(int h) { return 128u * h + 64u; }
   static constexpr uint32_t IDESC_NN = ptx::idesc_bf16_f32(T, T / 2, false);  // both operands K-major
   static constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(T, D, true);  // B MN-major
+  static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16_f32(T, D, true, true);  // A and B MN-major
+  // fused: the two dQ partial buffers follow the dK and dV accumulators
+  static constexpr uint32_t TMEM_DQ = 256u + 2u * D;
+  static_assert(!FUSED || TMEM_DQ + 2 * D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -171,12 +198,13 @@ __device__ __forceinline__ int key_limit(int i, int kv_len, bool causal) { retur
 // ------------------------------------------------------------------ dK, dV
 // KV tile kt of head bh; query tiles it = q_begin .. tiles-1 (causal: those at or
 // after the key tile). MODE selects the operand roles (see the file comment).
-template <int D, bool DKDV>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int D, bool DKDV, bool FUSED = false>
+__global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                        const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
-                       const BwdParams p) {
-  using C = BCfg<D>;
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  using C = BCfg<D, FUSED>;
+  static_assert(!FUSED || DKDV, "the fused schedule extends the dK/dV kernel");
   constexpr int STAGES = C::STAGES;
   // One issuer per half, each with its own accumulators (summed in the epilogue): for
   // the dQ kernel at D = 128, where the two halves' MMAs outrun one issuing thread
@@ -231,6 +259,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::mbar_init(bar(C::B_ACC), SPLIT ? 2 : 1);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     ptx::mbar_init(bar(C::B_DRAIN + 1), 1);
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(bar(C::B_DQFULL + x), 1);  // MMA commit
+      ptx::mbar_init(bar(C::B_DQFREE + x), 4);  // one arrival per drain warp
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -243,6 +275,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Fused: warpgroups 0-1 (elementwise) take registers from warpgroups 2-3 (producer,
+  // issuer, idle warp, drain warps); the sum equals the launch allocation.
+  if (warp >= 8) {
+  if constexpr (FUSED) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CTRL));
   if (warp == WARP_LOAD) {
     // ================================================================ producer (whole warp)
     bool ok = true;
@@ -280,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int u = max(0, issued - STAGES); u < issued; ++u) drain_wait(bar(C::B_FULL + u % STAGES), (u / STAGES) & 1);
     }
     __syncwarp();
-  } else if (warp >= WARP_MMA) {
+  } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
     // ================================================================ MMA issuers
     // Half h of streamed tile u: S_h(u) and dP_h(u) (64 streamed rows), then, once its
     // warpgroup has stored P / dS, the accumulations. SPLIT: warp WARP_MMA + h serves
@@ -297,6 +333,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t d_r0m = ptx::sdesc_sw128(s_base + C::OFF_R0, C::CHUNK_BYTES, 1024);  // MN-major view
       const uint64_t d_r1m = ptx::sdesc_sw128(s_base + C::OFF_R1, C::CHUNK_BYTES, 1024);
       auto koff16 = [](int kk) { return (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4); };
+      // fused: dQ_w = dS_w K into TMEM buffer w & 1; A = dS^T tile read MN-major (query
+      // halves 16 KB apart), B = the resident K tile read MN-major, 16 keys per MMA
+      const uint64_t d_ds = ptx::sdesc_sw128(s_base + C::OFF_DS, C::CHUNK_BYTES, 1024);
+      const uint64_t d_a0m = ptx::sdesc_sw128(s_base + C::OFF_A0, C::CHUNK_BYTES, 1024);
+      auto issue_dq = [&](int w) {
+        const uint32_t d_col = tmem + C::TMEM_DQ + (uint32_t)(w & 1) * D;
+#pragma unroll
+        for (int kk = 0; kk < T / 16; ++kk) {
+          const uint64_t ko = (uint64_t)((kk * 2048) >> 4);
+          ptx::mma_ss(d_col, d_ds + ko, d_a0m + ko, C::IDESC_DQ, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(C::B_DQFULL + (w & 1)));
+      };
       // X_h = A0 R0_h^T, Y_h = A1 R1_h^T (both operands K-major along d); rows 64h.. of
       // a streamed slab start 64h * 128 bytes in
       auto issue_sdp = [&](int u, int h) {
@@ -363,6 +412,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::tc_fence_after();
           issue_acc(u - 1, h);
           if (h == 1) ptx::mma_commit(bar(C::B_EMPTY + (u - 1) % STAGES));  // tile u-1's stage is consumed
+          if (FUSED && h == 1) {
+            // dS_{u-1} is complete in shared memory; its buffer's previous partial
+            // (tile u-3) must have been read out
+            const int w = u - 1;
+            if (w >= 2) {
+              ok = wait_bar(bar(C::B_DQFREE + (w & 1)), ((w >> 1) - 1) & 1, abort_flag);
+              if (!ok) break;
+              ptx::tc_fence_after();
+            }
+            issue_dq(w);
+          }
           if (u < n_s) issue_sdp(u, h);
         }
       }
@@ -374,7 +434,53 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (FUSED && warp >= WARP_DRAIN) {
+    // ================================================================ dQ drain (fused; warps 12-15)
+    // Thread = query row of the streamed tile = TMEM lane; warp w owns rows
+    // 32 (w % 4) .. + 31 and needs no other warp. Each partial goes TMEM -> registers ->
+    // the warp's swizzled fp32 staging tiles -> two TMA reduce-adds (columns 0-31 and
+    // 32-63, 32 rows each) into the fp32 accumulator; rows past n_q fall outside the
+    // tensor and are skipped. Lane 0 issues the reduces and, before the staging tiles
+    // are refilled, waits until the previous ones have read them.
+    const int quarter = warp & 3;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t stage = s_base + C::OFF_DQS + quarter * 2 * 4096;  // [2 column halves][32 rows][128 B]
+    bool ok = true;
+    for (int u = 0; u < n_s && ok; ++u) {
+      const int buf = u & 1;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_DQFULL + buf), (u >> 1) & 1, abort_flag));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (lane == 0) ptx::bulk_wait_read0();
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 16 columns at a time: column half c / 2, units 4 (c & 1) ..
+        uint32_t v[16];
+        ptx::tmem_ld16(tmem + lane_off + C::TMEM_DQ + (uint32_t)buf * D + c * 16, v);
+        ptx::tmem_wait_ld();
+        const uint32_t row = stage + (c >> 1) * 4096 + lane * 128;
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (uint32_t)((((c & 1) * 4 + x) ^ (lane & 7)) << 4)),
+                       "r"(v[4 * x]), "r"(v[4 * x + 1]), "r"(v[4 * x + 2]), "r"(v[4 * x + 3])
+                       : "memory");
+      }
+      ptx::tc_fence_before();
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(bar(C::B_DQFREE + buf));
+        const int y = (s_begin + u) * T + quarter * 32;
+        ptx::tma_reduce_add_3d(&tm_dq, stage, 0, y, bh);
+        ptx::tma_reduce_add_3d(&tm_dq, stage + 4096, 32, y, bh);
+        ptx::bulk_commit();
+      }
+    }
+    if (lane == 0) ptx::bulk_wait0();
+    __syncwarp();
+  }
   } else {
+    if constexpr (FUSED) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_EW));
     // ================================================================ elementwise warpgroups (warps 0-7)
     // Thread = own row (key for DKDV, query for dQ) = TMEM lane; warpgroup g takes half
     // g of every streamed tile (its rows 64g .. 64g + 63 = the columns of X_g, Y_g). No
@@ -452,6 +558,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // P^T over X_g and dS^T over Y_g (DKDV), or dS over X_g (dQ), at columns 16 ch:
         // already read (chunk ch covers columns 32 ch .. 32 ch + 31)
+        if (FUSED) {
+          // dS^T row of this key into the A tile of dQ_u = dS_u K: query half g, 16-byte
+          // unit c at (c ^ (key & 7)); the tile is free once dQ_{u-1} has been computed
+          if (ch == 0 && u > 0)
+            ok = __all_sync(0xffffffffu,
+                            wait_bar(bar(C::B_DQFULL + ((u - 1) & 1)), ((u - 1) >> 1) & 1, abort_flag));
+          if (ok) {
+            const uint32_t row = s_base + C::OFF_DS + g * C::CHUNK_BYTES + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (uint32_t)(((ch * 4 + j) ^ (r & 7)) << 4)),
+                           "r"(dw[4 * j]), "r"(dw[4 * j + 1]), "r"(dw[4 * j + 2]), "r"(dw[4 * j + 3])
+                           : "memory");
+          }
+        }
         if (DKDV) {
           asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
                        ::"r"(t_x + ch * 16), "r"(pw[0]), "r"(pw[1]), "r"(pw[2]), "r"(pw[3]), "r"(pw[4]),
@@ -464,6 +585,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                      "r"(dw[13]), "r"(dw[14]), "r"(dw[15]) : "memory");
       }
       ptx::tmem_wait_st();
+      if (!ok) break;
+      if (FUSED) ptx::fence_proxy_async_smem();  // dS^T stores before the dQ MMA reads them
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_PFULL + g));
     }
@@ -525,6 +648,28 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// dQ = scale * (the fp32 sum of the per-key-tile partials), rounded to bf16 once;
+// four elements per thread.
+__global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const float4* acc, uint2* dq, float scale,
+                                                                  long long n4) {
+  for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n4; i += (long long)gridDim.x * 256) {
+    const float4 a = acc[i];
+    dq[i] = make_uint2(ptx::pack_bf16x2(a.x * scale, a.y * scale), ptx::pack_bf16x2(a.z * scale, a.w * scale));
+  }
+}
+
+// The fp32 dQ accumulator [bh][n][64] as the reduce target: boxes of 32 columns
+// (128 bytes) x 32 rows, 128-byte swizzle.
+CUresult encode_acc(PFN_encodeTiled enc, CUtensorMap* map, const float* base, int n, int bh) {
+  cuuint64_t dims[3] = {64, (cuuint64_t)n, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {64 * 4, (cuuint64_t)64 * 4 * (cuuint64_t)n};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 CUresult encode(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int d, int n, int bh) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)n};
@@ -535,28 +680,43 @@ CUresult encode(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int d, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D, bool DKDV>
+template <int D, bool DKDV, bool FUSED = false>
 int set_smem_attr() {
   static std::atomic<bool> done[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   if (!done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<D, DKDV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BCfg<D>::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<D, DKDV, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BCfg<D, FUSED>::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
     done[dev].store(true, std::memory_order_release);
   }
   return ATTN_OK;
 }
 
+// dq_acc: the fp32 dQ accumulator of the fused schedule, or null for the
+// deterministic one.
 template <int D>
-int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats) {
+int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_acc) {
   const int BH = a.B * a.H;
-  CUtensorMap mq, mk, mv, mdo;
+  const bool fused = dq_acc != nullptr;
+  CUtensorMap mq, mk, mv, mdo, macc;
   if (encode(enc, &mq, a.q, D, a.n_q, BH) != CUDA_SUCCESS || encode(enc, &mk, a.k, D, a.n_k, BH) != CUDA_SUCCESS ||
       encode(enc, &mv, a.v, D, a.n_k, BH) != CUDA_SUCCESS || encode(enc, &mdo, a.dout, D, a.n_q, BH) != CUDA_SUCCESS)
     return ATTN_ERR_UNSUPPORTED;
-  if (set_smem_attr<D, true>() != ATTN_OK || set_smem_attr<D, false>() != ATTN_OK) return ATTN_ERR_CUDA;
+  if (fused && encode_acc(enc, &macc, dq_acc, a.n_q, BH) != CUDA_SUCCESS) return ATTN_ERR_UNSUPPORTED;
+  if (!fused) macc = mq;  // not read by the deterministic kernels
+  if (fused) {
+    if constexpr (D == 64) {
+      if (set_smem_attr<D, true, true>() != ATTN_OK) return ATTN_ERR_CUDA;
+    } else {
+      return ATTN_ERR_UNSUPPORTED;
+    }
+  } else if (set_smem_attr<D, true>() != ATTN_OK || set_smem_attr<D, false>() != ATTN_OK) {
+    return ATTN_ERR_CUDA;
+  }
+  if (fused && cudaMemsetAsync(dq_acc, 0, (size_t)BH * a.n_q * D * sizeof(float), a.stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   const int q_tiles = (a.n_q + T - 1) / T;
   const long long rows = (long long)BH * q_tiles * T;
   if ((rows + 7) / 8 > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
@@ -580,7 +740,21 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats) {
   p.tiles = (a.n_k + T - 1) / T;
   long long grid = (long long)BH * p.tiles;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_bwd_tc_kernel<D, true><<<(unsigned)grid, THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mk, mv, mq, mdo, p);
+  if (fused) {
+    if constexpr (D == 64) {
+      using CF = BCfg<D, true>;
+      attn_bwd_tc_kernel<D, true, true><<<(unsigned)grid, CF::THREADS, CF::SMEM_BYTES, a.stream>>>(mk, mv, mq, mdo,
+                                                                                                   macc, p);
+      if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+      const long long n4 = (long long)BH * a.n_q * D / 4;
+      const long long blocks = std::min<long long>((n4 + 255) / 256, 152LL * 8);
+      attn_bwd_dq_convert_kernel<<<(unsigned)blocks, 256, 0, a.stream>>>(
+          reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(a.dq), a.scale, n4);
+      return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+  }
+  attn_bwd_tc_kernel<D, true><<<(unsigned)grid, BCfg<D>::THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mk, mv, mq, mdo,
+                                                                                                  macc, p);
   if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   // dQ: own = query tiles; A0 = Q, A1 = dO; streamed R0 = K, R1 = V
   p.g0 = static_cast<uint16_t*>(a.dq);
@@ -588,19 +762,27 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats) {
   p.tiles = (a.n_q + T - 1) / T;
   grid = (long long)BH * p.tiles;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_bwd_tc_kernel<D, false><<<(unsigned)grid, THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mq, mdo, mk, mv, p);
+  attn_bwd_tc_kernel<D, false><<<(unsigned)grid, BCfg<D>::THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mq, mdo, mk, mv,
+                                                                                                   macc, p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
 
-// per (b, h) and 128-row query tile: -lse log2(e) and -D of its rows, 2 x 128 floats
-size_t bwd_workspace_bytes(int B, int H, int n_q) { return (size_t)B * H * ((n_q + T - 1) / T) * 2 * T * sizeof(float); }
+bool bwd_fused(int d, int flags) { return d == 64 && !(flags & ATTN_BWD_DETERMINISTIC); }
+
+// per (b, h) and 128-row query tile: -lse log2(e) and -D of its rows, 2 x 128 floats;
+// then, for the fused schedule, the fp32 dQ accumulator [B h][n_q][64]
+size_t bwd_workspace_bytes(int B, int H, int n_q, int d, int flags) {
+  const size_t stats = (size_t)B * H * ((n_q + T - 1) / T) * 2 * T * sizeof(float);
+  return stats + (bwd_fused(d, flags) ? (size_t)B * H * n_q * 64 * sizeof(float) : 0);
+}
 
 int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace) {
   float* stats = static_cast<float*>(workspace);
-  if (a.d == 64) return launch_bwd<64>(a, enc, stats);
-  if (a.d == 128) return launch_bwd<128>(a, enc, stats);
+  float* dq_acc = bwd_fused(a.d, a.flags) ? stats + (size_t)a.B * a.H * ((a.n_q + T - 1) / T) * 2 * T : nullptr;
+  if (a.d == 64) return launch_bwd<64>(a, enc, stats, dq_acc);
+  if (a.d == 128) return launch_bwd<128>(a, enc, stats, nullptr);
   return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -75,6 +75,7 @@ struct BwdArgs {
   int mask_mode;
   const int32_t* key_lens;
   cudaStream_t stream;
+  int flags = 0;  // ATTN_BWD_DETERMINISTIC
 };
 
 // Validated arguments of one multi-head layer call (d_k == d_v == d).
@@ -106,8 +107,9 @@ size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d);  // attn
 int launch_attn_decode(const DecodeArgs& a, void* workspace);            // attn_decode.cu
 int launch_attn_decode_noalloc(const DecodeArgs& a);                     // attn_decode.cu
 int read_decode_fault_word(int clear, uint32_t* out);                   // attn_decode.cu
-size_t bwd_workspace_bytes(int B, int H, int n_q);                       // attn_bwd.cu
+size_t bwd_workspace_bytes(int B, int H, int n_q, int d, int flags);     // attn_bwd.cu
 int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_bwd.cu
+bool bwd_fused(int d, int flags);                                        // attn_bwd.cu
 int read_bwd_fault_word(int clear, uint32_t* out);                       // attn_bwd.cu
 size_t mha_workspace_bytes(int B, int n_q, int n_k, int H, int d);         // attn_mha.cu
 int launch_attn_mha(const MhaArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_mha.cu
