@@ -57,12 +57,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "attn_fwd_tc_kernel": ("attn_fwd_tc.cu", "ptx_sm103.cuh"),
     "attn_decode_split_kernel": ("attn_decode.cu", "ptx_sm103.cuh"),
+    "attn_bwd_tc_kernel": ("attn_bwd.cu", "ptx_sm103.cuh"),
 }
 NCU_TRAFFIC = {
     # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
     ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "4146bd9c4867a47d"): 142052608,
     # profiles/attn_decode_split_kernel_decode_b16_h16_q1_k8192_d64.md (split kernel only)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_split_kernel", "72652789c3570524"): 424460032,
+    # profiles/attn_bwd_tc_kernel_long_causal_b2_h16_n8192_d64.md (the fused d = 64 kernel)
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "a1b730ba328d5ec0"): 1064478976,
 }
 
 
@@ -540,9 +543,15 @@ def run_ours_grad(args, w):
         return None
     peaks, peak_src = load_peaks()
     achieved = flops_step / (ms_per_step / 1e3) / 1e12
+    fused = w.d_k == 64
+    src_hash = kernel_source_hash("attn_bwd_tc_kernel")
     roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": float(peaks["bf16_tflops"]),
             "unit": "TFLOP/s", "peak_source": f"bf16_tflops (burst) of {peak_src}",
-            "kernel": "attn_bwd (dot kernel + dK/dV kernel + dQ kernel, timed together)", "traffic": None}
+            "kernel": ("attn_bwd fused schedule (memset, dot kernel, fused dK/dV/dQ kernel, dQ conversion; "
+                       "timed together)" if fused else
+                       "attn_bwd (dot kernel + dK/dV kernel + dQ kernel, timed together)"),
+            "traffic": NCU_TRAFFIC.get((w.name, "attn_bwd_tc_kernel", src_hash)) if fused else None,
+            "kernel_source": src_hash}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     line = {
         "metric": "attention bwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak",
@@ -550,6 +559,8 @@ def run_ours_grad(args, w):
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, {"pass": "gradients (attn_bwd)",
+                                "schedule": ("fused: five products once, dQ by TMA reduce-add" if fused else
+                                             "deterministic: dK/dV kernel + dQ kernel, seven products"),
                                 "flops": "algorithmic: 2*(3*d_k+2*d_v) per legal (query, key) pair",
                                 "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB memset)",
                                 "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
