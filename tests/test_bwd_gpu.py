@@ -39,6 +39,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from transformer_scaled_dot_mha_gb300 import attn, workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -89,11 +90,13 @@ def run_bwd(q, k, v, dout, scale, mask, lens, flags=0):
     return (f(dq), f(dk), f(dv)), f(out)
 
 
-def bounds(orc, q, k, v, dout, scale, mask, lens, ref, out_dev):
+def bounds(orc, q, k, v, dout, scale, mask, lens, ref, out_dev, P=None, lse=None):
     """(worst-case bounds, quadrature bounds) of the CUDA path's error, per element
-    (module docstring)."""
-    P = orc.attention_weights(q, k, scale, mask, lens)
-    _, lse = orc.attention(q, k, v, scale, mask, lens)
+    (module docstring). P and lse, the oracle's weights and log-sum-exp, may be given."""
+    if P is None:
+        P = orc.attention_weights(q, k, scale, mask, lens)
+    if lse is None:
+        _, lse = orc.attention(q, k, v, scale, mask, lens)
     Q, K, V, G = (bits_to_f64(x) for x in (q, k, v, dout))
     dq_r, dk_r, dv_r = ref
     d, n_q, n_k = Q.shape[-1], Q.shape[-2], K.shape[-2]
@@ -235,3 +238,26 @@ def test_bwd_rejects_small_workspace():
     with pytest.raises(attn.AttnError) as e:
         attn.attn_bwd(qd, kd, vd, qd, gd, lse, torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd), ws)
     assert e.value.status == attn.ATTN_ERR_INVALID
+
+
+@pytest.mark.parametrize("name,heads", [("long_causal_b2_h16_n8192_d64", [(0, 3), (1, 14)]),
+                                        ("long_none_b2_h16_n8192_d128", [(1, 7)])])
+def test_bwd_full_size_sampled_heads(orc, name, heads):
+    """The bench's gradient workloads at full size (B 2, h 16, n 8192), in the launch
+    configuration it times: the fused schedule at d = 64, the deterministic one at
+    d = 128. Whole heads are sampled and checked element by element against the
+    oracle's gradients of that head (its matrix form: one head of n = 8192 is a few
+    BLAS products), with the derived bounds."""
+    w = W.WORKLOADS[name]
+    q, k, v, kl = W.make_inputs(w)
+    dout = W.make_grad_output(w)
+    got, out_dev = run_bwd(q, k, v, dout, w.scale, w.mask_mode, kl)
+    for b, h in heads:
+        sl = lambda a: np.ascontiguousarray(a[b:b + 1, h:h + 1])
+        hq, hk, hv, hg = sl(q), sl(k), sl(v), sl(dout)
+        ref = oracle.attention_bwd_matrix_form(hq, hk, hv, hg, w.scale, w.mask_mode, None)
+        _, lse, P = oracle.attention_matrix_form(hq, hk, hv, w.scale, w.mask_mode, None)
+        bnd = bounds(orc, hq, hk, hv, hg, w.scale, w.mask_mode, None, ref, sl(out_dev), P=P, lse=lse)
+        head_got = tuple(sl(x) for x in got)
+        RESULTS.append(((1, 1, w.n_q, w.n_k, w.d_k, w.mask_mode), ratios(head_got, ref, bnd)))
+        check(head_got, ref, bnd)
