@@ -247,6 +247,34 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              void* stream);
 
 /*
+ * attn_bwd_host_workspace_size -- bytes of device workspace attn_bwd_host needs for
+ * this shape, head size, mask and flags (four chunk slots of the nine per-head tensors
+ * and their gradient workspace, plus the key lengths). Returns 0 for an invalid shape,
+ * head size, mask or flag. Depends only on the arguments.
+ */
+size_t attn_bwd_host_workspace_size(int B, int h, int n_q, int n_k, int d, int mask_mode, int flags);
+
+/*
+ * attn_bwd_host -- attn_bwd for operands that live in HOST memory (a training step
+ * whose tensors are on the host). Same gradients, schedules, flags and numerics as
+ * attn_bwd: the same kernels run on each chunk of heads (dk and dv bit-identical to
+ * attn_bwd on the same data; dq as well with ATTN_BWD_DETERMINISTIC).
+ *   q, k, v, out, dout, lse, key_lens: host memory, read;   dq, dk, dv: host memory,
+ *   written. Page-locked (pinned) host memory is strongly recommended.
+ *   workspace: device scratch of at least attn_bwd_host_workspace_size(B, h, n_q, n_k,
+ *   d_k, mask_mode, flags) bytes, 256-byte aligned, owned by the caller.
+ * The flattened (b, h) head range is cut into chunks whose host-to-device copies,
+ * gradient kernels and device-to-host copies run on the library's own streams through
+ * a four-slot ring in the workspace, as in attn_fwd_host. The call is asynchronous on
+ * `stream` and ordered with it at both ends; the host buffers must stay valid (and the
+ * inputs unmodified) until `stream` reaches the end of the call. Errors as attn_bwd.
+ */
+int attn_bwd_host(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
+                  int mask_mode, const int32_t* key_lens, int flags, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/*
  * attn_mha_workspace_size -- bytes of device workspace attn_mha_fwd needs: the
  * projected Q', K', V' and the concatenated heads (bf16) plus 32 MiB of GEMM
  * workspace. Returns 0 for an invalid or unsupported shape.

@@ -183,3 +183,31 @@ def test_host_forward_workspace_and_argument_checks(L):
     assert call(d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED
     assert call(d_v=128) == attn.ATTN_ERR_UNSUPPORTED
     assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID
+
+
+def test_host_gradients_workspace_and_argument_checks(L):
+    ws = attn.attn_bwd_host_workspace_size
+    # 6 heads of n = 300, d = 64: one chunk. One slot of Q, O, dO, dQ and K, V, dK, dV
+    # (6*300*64*2 = 230400 bytes each), lse 6*300*4 = 7200 -> 7424, and the gradient
+    # workspace of 6 heads: 3 tiles x 1024 bytes of statistics per head, plus the fused
+    # schedule's fp32 dQ (300*64*4 per head); after 2 key lengths padded to 256 bytes.
+    assert ws(2, 3, 300, 300, 64, 0, 0) == 256 + 8 * 230400 + 7424 + 6 * (3072 + 76800)
+    assert ws(2, 3, 300, 300, 64, 0, attn.BWD_DETERMINISTIC) == 256 + 8 * 230400 + 7424 + 6 * 3072
+    assert ws(1, 1, 8, 8, 96, 0, 0) == 0 and ws(1, 1, 8, 8, 64, 4, 0) == 0 and ws(1, 1, 8, 8, 64, 0, 2) == 0
+    need = ws(2, 3, 300, 300, 64, 1, 0)
+    ok = dict(q=16, k=32, v=48, out=64, dout=80, lse=96, dq=112, dk=128, dv=144, B=2, h=3, n_q=300, n_k=300,
+              d_k=64, d_v=64, scale=0.125, mask=1, lens=None, flags=0, ws=256, nbytes=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.attn_bwd_host(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"],
+                               a["B"], a["h"], a["n_q"], a["n_k"], a["d_k"], a["d_v"], a["scale"], a["mask"],
+                               a["lens"], a["flags"], a["ws"], a["nbytes"], None)
+    assert call(nbytes=need - 1) == attn.ATTN_ERR_INVALID      # workspace too small
+    assert call(ws=272) == attn.ATTN_ERR_INVALID               # workspace not 256-byte aligned
+    for name in ("dout", "lse", "dq", "dk", "dv", "ws"):
+        assert call(**{name: None}) == attn.ATTN_ERR_INVALID
+    assert call(flags=2) == attn.ATTN_ERR_INVALID
+    assert call(n_k=200) == attn.ATTN_ERR_INVALID              # causal needs n_q == n_k
+    assert call(mask=2) == attn.ATTN_ERR_INVALID               # key padding without key_lens
+    assert call(d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED

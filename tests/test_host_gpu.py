@@ -127,3 +127,65 @@ def test_full_size_workloads(name):
     w = W.WORKLOADS[name]
     q, k, v, kl = W.make_inputs(w)
     assert_identical(*run_both(q, k, v, kl, w.scale, w.mask_mode))
+
+
+# ------------------------------------------------------------------ gradients on host operands
+BWD_CASES = [
+    # (B, H, n, d, mask, flags); plans from 8 MiB minimum chunks and the copy/kernel time ratio
+    (7, 4, 2048, 64, C | P, 0),                        # ramp 7, 11, 10: the 11 is three rectangles; fused
+    (7, 4, 2048, 64, C | P, attn.BWD_DETERMINISTIC),   # the same, deterministic schedule
+    (5, 6, 2048, 128, 0, 0),                           # ramp 4, 8, 9, 5, 4: five chunks, four slots; d = 128
+    (2, 3, 300, 64, C | P, 0),                         # ragged rows, one chunk
+]
+
+
+def run_bwd_both(q, k, v, g, kl, scale, mode, flags):
+    """attn_bwd_host on pinned host tensors and attn_bwd on device copies, both given the
+    device forward's out and lse."""
+    B, H, n, d = q.shape
+    qh, kh, vh, gh = (host_bf16(a) for a in (q, k, v, g))
+    kl_d = torch.from_numpy(kl.copy()).cuda() if mode & P else None
+    qd, kd, vd, gd = qh.cuda(), kh.cuda(), vh.cuda(), gh.cuda()
+    out_d, lse_d = attn.attention(qd, kd, vd, scale, mode, kl_d, with_lse=True)
+    grads_d = [torch.empty_like(t) for t in (qd, kd, vd)]
+    ws_d = torch.empty(attn.attn_bwd_workspace_size(B, H, n, d, flags), dtype=torch.uint8, device="cuda")
+    attn.attn_bwd(qd, kd, vd, out_d, gd, lse_d, *grads_d, ws_d, scale, mode, kl_d, flags=flags)
+    outh, lseh = out_d.cpu().pin_memory(), lse_d.cpu().pin_memory()
+    klh = torch.from_numpy(kl.copy()).pin_memory() if mode & P else None
+    grads_h = [torch.full(t.shape, float("nan"), dtype=torch.bfloat16).pin_memory() for t in (qd, kd, vd)]
+    ws_h = torch.empty(attn.attn_bwd_host_workspace_size(B, H, n, n, d, mode, flags), dtype=torch.uint8,
+                       device="cuda")
+    attn.attn_bwd_host(qh, kh, vh, outh, gh, lseh, *grads_h, ws_h, scale, mode, klh, flags=flags)
+    torch.cuda.synchronize()
+    return [t.cpu() for t in grads_d], grads_h
+
+
+def assert_bwd_match(grads_d, grads_h, bitwise_dq):
+    U = 2.0 ** -8
+    for name, gd, gh in zip(("dq", "dk", "dv"), grads_d, grads_h):
+        if name != "dq" or bitwise_dq:
+            assert torch.equal(gd.view(torch.int16), gh.view(torch.int16)), f"{name} differs from attn_bwd"
+        else:  # the fused schedule's dq: reduce order varies between the two calls
+            a, b = gd.float(), gh.float()
+            assert torch.all((a - b).abs() <= 4 * U * a.abs() + 1e-6), f"dq differs by {(a - b).abs().max()}"
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "B{}_H{}_n{}_d{}_m{}_f{}".format(*c))
+def test_host_gradients_equal_device_gradients(case):
+    B, H, n, d, mode, flags = case
+    w = W.WORKLOADS["decoder_causal_b16_h8_n512_d64"]
+    q, k, v, _ = W.make_inputs(w, seed=31, B=B, H=H, n_q=n, n_k=n, d_k=d, d_v=d)
+    g = W.make_grad_output(w, seed=31, B=B, H=H, n_q=n, d_v=d)
+    rng = np.random.Generator(np.random.PCG64(12))
+    kl = rng.integers(1, n, size=B, endpoint=True).astype(np.int32) if mode & P else np.full(B, n, np.int32)
+    grads_d, grads_h = run_bwd_both(q, k, v, g, kl, d ** -0.5, mode, flags)
+    assert_bwd_match(grads_d, grads_h, bitwise_dq=(d == 128 or flags & attn.BWD_DETERMINISTIC))
+
+
+def test_host_gradients_full_size():
+    """The bench's gradient workload: eight equal chunks of 4 heads of n = 8192, fused."""
+    w = W.WORKLOADS["long_causal_b2_h16_n8192_d64"]
+    q, k, v, kl = W.make_inputs(w)
+    g = W.make_grad_output(w)
+    grads_d, grads_h = run_bwd_both(q, k, v, g, kl, w.scale, w.mask_mode, 0)
+    assert_bwd_match(grads_d, grads_h, bitwise_dq=False)

@@ -58,6 +58,11 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp,
                                ctypes.c_size_t, vp]
         L.attn_bwd.restype = i
+        L.attn_bwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        L.attn_bwd_host_workspace_size.restype = ctypes.c_size_t
+        L.attn_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp,
+                                    ctypes.c_size_t, vp]
+        L.attn_bwd_host.restype = i
         L.attn_mha_workspace_size.argtypes = [i, i, i, i, i, i]
         L.attn_mha_workspace_size.restype = ctypes.c_size_t
         L.attn_mha_fwd.argtypes = [vp] * 11 + [i, i, i, i, i, i, i, f, i, vp, vp, ctypes.c_size_t, vp]
@@ -279,6 +284,40 @@ def attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, scale=None, mask_mo
                         _ptr(workspace), nbytes, _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_host_workspace_size(B, H, n_q, n_k, d, mask_mode=MASK_NONE, flags=0) -> int:
+    return int(lib().attn_bwd_host_workspace_size(B, H, n_q, n_k, d, int(mask_mode), int(flags)))
+
+
+def attn_bwd_host(q, k, v, out, dout, lse, dq, dk, dv, workspace, scale=None, mask_mode=MASK_NONE, key_lens=None,
+                  stream=None, flags=0):
+    """attn_bwd on HOST tensors (pinned recommended): q, k, v, out, dout (bf16), lse
+    (float32) and key_lens are read and dq, dk, dv written in host memory; the chunked
+    copy/compute pipeline runs on the GPU with ``workspace`` (a CUDA uint8 tensor of
+    attn_bwd_host_workspace_size bytes) and is asynchronous on ``stream``."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous 4-D host bf16 tensor, got {t.dtype} {tuple(t.shape)}")
+    B, H, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    if (k.shape != (B, H, n_k, d_k) or v.shape != (B, H, n_k, d_v) or out.shape != (B, H, n_q, d_v)
+            or dout.shape != out.shape or dq.shape != q.shape or dk.shape != k.shape or dv.shape != v.shape):
+        raise ValueError("shape mismatch between q, k, v, out, dout and the gradients")
+    if lse.dtype != torch.float32 or lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, n_q):
+        raise ValueError("lse must be a contiguous host float32 tensor of shape [B, H, n_q]")
+    if key_lens is not None and (key_lens.dtype != torch.int32 or key_lens.is_cuda or key_lens.shape != (B,)):
+        raise ValueError("key_lens must be a host int32 tensor of shape [B]")
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    st = lib().attn_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                             _ptr(dv), B, H, n_q, n_k, d_k, d_v, float(scale), int(mask_mode), _ptr(key_lens),
+                             int(flags), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_host")
     return dq, dk, dv
 
 

@@ -175,6 +175,32 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   return attn::launch_attn_bwd(a, enc, workspace);
 }
 
+size_t attn_bwd_host_workspace_size(int B, int h, int n_q, int n_k, int d, int mask_mode, int flags) {
+  if (B <= 0 || h <= 0 || n_q <= 0 || n_k <= 0 || (d != 64 && d != 128)) return 0;
+  if (mask_mode < 0 || mask_mode > (ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return 0;
+  if (flags & ~ATTN_BWD_DETERMINISTIC) return 0;
+  const long long bh = (long long)B * h;
+  if (bh > 0x7fffffffLL || bh * (n_q > n_k ? n_q : n_k) > (1LL << 40) / d) return 0;
+  return attn::bwd_host_workspace_bytes(B, h, n_q, n_k, d, mask_mode, flags);
+}
+
+int attn_bwd_host(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k, int d_k, int d_v, float scale,
+                  int mask_mode, const int32_t* key_lens, int flags, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  int st = check_common(q, k, v, out, lse, B, h, n_q, n_k, d_k, d_v, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (!dout || !lse || !dq || !dk || !dv || !workspace || !aligned(workspace, 256)) return ATTN_ERR_INVALID;
+  if (flags & ~ATTN_BWD_DETERMINISTIC) return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < attn::bwd_host_workspace_bytes(B, h, n_q, n_k, d_k, mask_mode, flags)) return ATTN_ERR_INVALID;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::BwdArgs a{q, k, v, out, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, mask_mode, key_lens,
+                  static_cast<cudaStream_t>(stream), flags};
+  return attn::launch_attn_bwd_host(a, enc, workspace);
+}
+
 size_t attn_mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d) {
   if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || (d != 64 && d != 128)) return 0;
   if ((long long)B * (n_q > n_k ? n_q : n_k) * h * d > (1LL << 38)) return 0;

@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kSlots = 4;
-constexpr int kMaxChunks = 64;
+constexpr int kMaxChunks = kMaxHostChunks;
 constexpr size_t kAlign = 256;
 constexpr size_t kMinChunkBytes = size_t(8) << 20;  // host-to-device bytes of the smallest chunk
 // Rates used only to choose the chunk plan (results do not depend on it): the
@@ -77,35 +77,11 @@ HeadBytes head_bytes(int n_q, int n_k, int d) {
   return {(size_t)n_q * d * 2, (size_t)n_k * d * 2, (size_t)n_q * d * 2, (size_t)n_q * 4};
 }
 
-// Chunk sizes (in heads) for bh heads, each at least min_heads, the remainder merged
-// into the last chunk when it would fall below that.
-//  - Transfer-bound (a head's kernel time well under its copy time, e.g. causal or
-//    short sequences): a ramp that starts at min_heads and doubles but never takes
-//    more than half of what is left, so the sizes rise and then fall by halves. Only
-//    the first copy and the last kernel + copy back overlap nothing, so both are small.
-//  - Otherwise: eight equal chunks, each a fraction of a wave of CTAs, whose kernels
-//    interleave on the slot streams and keep every SM busy.
+// The forward's chunk plan (see plan_chunks).
 int chunk_plan(long long bh, const HeadBytes& hb, int n_q, int n_k, int d, bool causal,
                long long sizes[kMaxChunks]) {
-  const size_t in_bytes = hb.q + 2 * hb.kv;
-  long long min_heads = (long long)((kMinChunkBytes + in_bytes - 1) / in_bytes);
-  if (min_heads < 1) min_heads = 1;
   const double pairs = causal ? 0.5 * n_q * (n_q + 1.0) : (double)n_q * n_k;
-  const double kernel_us = 4.0 * d * pairs / kKernelFlopsPerUs;
-  const double copy_us = (double)(in_bytes + hb.o) / kLinkBytesPerUs;
-  const bool ramped = kernel_us < 0.6 * copy_us;
-  int n = 0;
-  long long left = bh, ramp = min_heads;
-  while (left > 0) {
-    long long c = ramped ? (left + 1) / 2 : (bh + 7) / 8;
-    if (ramped && c > ramp) c = ramp;
-    if (c < min_heads) c = min_heads;
-    if (left - c < min_heads || n == kMaxChunks - 1) c = left;
-    sizes[n++] = c;
-    left -= c;
-    if (ramp < bh) ramp *= 2;
-  }
-  return n;
+  return plan_chunks(bh, hb.q + 2 * hb.kv, hb.o, 4.0 * d * pairs / kKernelFlopsPerUs, sizes);
 }
 
 // Bytes of a slot holding `heads` heads: q, k, v, out, lse, each 256-byte aligned.
@@ -121,6 +97,34 @@ void slot_caps(const long long* sizes, int n, long long caps[kSlots]) {
 }
 
 }  // namespace
+
+// Chunk sizes (in heads) for bh heads of in_bytes copied in and out_bytes copied back
+// each, whose kernel takes about kernel_us: every chunk at least kMinChunkBytes of
+// input, the remainder merged into the last chunk when it would fall below that.
+//  - Transfer-bound (a head's kernel time well under its copy time, e.g. causal or
+//    short sequences): a ramp that starts at the minimum and doubles but never takes
+//    more than half of what is left, so the sizes rise and then fall by halves. Only
+//    the first copy and the last kernel + copy back overlap nothing, so both are small.
+//  - Otherwise: eight equal chunks, each a fraction of a wave of CTAs, whose kernels
+//    interleave on the slot streams and keep every SM busy.
+int plan_chunks(long long bh, size_t in_bytes, size_t out_bytes, double kernel_us, long long* sizes) {
+  long long min_heads = (long long)((kMinChunkBytes + in_bytes - 1) / in_bytes);
+  if (min_heads < 1) min_heads = 1;
+  const double copy_us = (double)(in_bytes + out_bytes) / kLinkBytesPerUs;
+  const bool ramped = kernel_us < 0.6 * copy_us;
+  int n = 0;
+  long long left = bh, ramp = min_heads;
+  while (left > 0) {
+    long long c = ramped ? (left + 1) / 2 : (bh + 7) / 8;
+    if (ramped && c > ramp) c = ramp;
+    if (c < min_heads) c = min_heads;
+    if (left - c < min_heads || n == kMaxHostChunks - 1) c = left;
+    sizes[n++] = c;
+    left -= c;
+    if (ramp < bh) ramp *= 2;
+  }
+  return n;
+}
 
 size_t host_workspace_bytes(int B, int H, int n_q, int n_k, int d, int mask_mode) {
   const HeadBytes hb = head_bytes(n_q, n_k, d);
@@ -186,15 +190,8 @@ int launch_attn_host(const TcArgs& a, PFN_encodeTiled enc, void* workspace) {
       return ATTN_ERR_CUDA;
     // cover heads [f0, f1) with rectangles of (batches x heads)
     for (long long f = f0; f < f1;) {
-      const int b = (int)(f / a.H), h = (int)(f % a.H);
-      int pb, ph;  // batches and heads per batch of this rectangle
-      if (h != 0 || f1 - f < a.H) {
-        pb = 1;
-        ph = (int)((f1 - f < a.H - h) ? f1 - f : a.H - h);
-      } else {
-        pb = (int)((f1 - f) / a.H);
-        ph = a.H;
-      }
+      int b, pb, ph;  // first batch, batches and heads per batch of this rectangle
+      head_rect(f, f1, a.H, b, pb, ph);
       const long long r = f - f0;  // heads into the slot
       TcArgs t{sq + r * hb.q, sk + r * hb.kv, sv + r * hb.kv, so + r * hb.o,
                a.lse ? reinterpret_cast<float*>(sl + r * hb.l) : nullptr, pb, ph, a.n_q, a.n_k, a.d, a.scale,

@@ -110,9 +110,28 @@ int read_decode_fault_word(int clear, uint32_t* out);                   // attn_
 size_t bwd_workspace_bytes(int B, int H, int n_q, int d, int flags);     // attn_bwd.cu
 int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_bwd.cu
 bool bwd_fused(int d, int flags);                                        // attn_bwd.cu
+size_t bwd_host_workspace_bytes(int B, int H, int n_q, int n_k, int d, int mask_mode, int flags);  // attn_bwd_host.cu
+int launch_attn_bwd_host(const BwdArgs& a, PFN_encodeTiled enc, void* workspace);                 // attn_bwd_host.cu
 int read_bwd_fault_word(int clear, uint32_t* out);                       // attn_bwd.cu
 size_t mha_workspace_bytes(int B, int n_q, int n_k, int H, int d);         // attn_mha.cu
 int launch_attn_mha(const MhaArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_mha.cu
+// Host-operand pipelines (attn_host.cu, attn_bwd_host.cu): chunks of the flattened
+// [B, h] head range, each covered by at most three (batches x heads) rectangles.
+constexpr int kMaxHostChunks = 64;
+int plan_chunks(long long bh, size_t in_bytes, size_t out_bytes, double kernel_us, long long* sizes);  // attn_host.cu
+// The rectangle that starts at flattened head f of [f, f1): batch b, pb whole batches of
+// H heads, or (pb = 1) ph heads of batch b up to the end of the batch or of the range.
+inline void head_rect(long long f, long long f1, int H, int& b, int& pb, int& ph) {
+  b = (int)(f / H);
+  const int h = (int)(f % H);
+  if (h != 0 || f1 - f < H) {
+    pb = 1;
+    ph = (int)((f1 - f < H - h) ? f1 - f : H - h);
+  } else {
+    pb = (int)((f1 - f) / H);
+    ph = H;
+  }
+}
 size_t host_workspace_bytes(int B, int H, int n_q, int n_k, int d, int mask_mode);  // attn_host.cu
 int launch_attn_host(const TcArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_host.cu
 
