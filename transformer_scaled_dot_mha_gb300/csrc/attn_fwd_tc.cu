@@ -108,8 +108,9 @@ struct Cfg {
   static constexpr int WARP_LOAD = SOFTMAX_WARPS;
   static constexpr int WARP_MMA0 = SOFTMAX_WARPS + 1;  // MMA issuer role 0 (S of Q tile 0)
   static constexpr int THREADS = SINGLE ? 256 : SEP_P ? 512 : 384;
-  static constexpr int REGS_CONTROL = SEP_P ? 40 : 56;
-  static constexpr int REGS_SOFTMAX = SEP_P ? 216 : 224;
+  // d = 128: 72 registers keep the single MMA issuer's loop free of spills
+  static constexpr int REGS_CONTROL = SEP_P ? 40 : 72;
+  static constexpr int REGS_SOFTMAX = 216;
   static constexpr int LAUNCH_REGS = (65536 / (THREADS * CTAS_PER_SM)) & ~7;  // 128 or 168 per thread
   static_assert((THREADS - SOFTMAX_THREADS) * REGS_CONTROL + SOFTMAX_THREADS * REGS_SOFTMAX == THREADS * LAUNCH_REGS,
                 "register split");
