@@ -61,7 +61,7 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "fef4e184dfd4da0a"): 141860096,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "f04eccf88779d958"): 143091968,
     # profiles/attn_decode_split_kernel_decode_b16_h16_q1_k8192_d64.md (split kernel only)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_split_kernel", "e3aceb2267d93ef1"): 424043008,
     # profiles/attn_bwd_tc_kernel_long_causal_b2_h16_n8192_d64.md (the fused d = 64 kernel)
