@@ -167,7 +167,9 @@ size_t attn_decode_workspace_size(int B, int h, int n_q, int n_max, int d);
  *           must not share a workspace.
  * Supported: 1 <= n_q <= 16, d in {64, 128}, B*h <= 65535. Pointers 16-byte
  * aligned. fp32 arithmetic throughout (scores, exp2, sums, P.V); the output is
- * rounded to bf16 once. Asynchronous on `stream`; two kernels are launched.
+ * rounded to bf16 once. Asynchronous on `stream`; two kernels are launched (one
+ * warp per cache chunk for n_q = 1, one block per cache range for n_q > 1; then the
+ * merge).
  */
 int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
                 int B, int h, int n_q, int n_max, int d, float scale,

@@ -8,7 +8,10 @@
 // per head (rockcohen.cc section 5.1).
 //
 // The work per query is tiny (a dot product and an axpy per cached key) while the
-// cache is large, so the step is bound by reading K and V from HBM once. Design:
+// cache is large, so the step is bound by reading K and V from HBM once. One query
+// per (b, h) (the usual generation step) runs attn_decode_warp_kernel: the cache is
+// cut into chunks, one independent warp per chunk (see there). Two to sixteen
+// queries run the block kernel:
 //   * split-K: the cache of each (b, h) is cut into `splits` ranges of whole
 //     128-key tiles, one CTA per (range, b*h), enough CTAs to fill every SM;
 //   * each CTA streams its 128-key K and V tiles with bulk asynchronous copies
@@ -17,7 +20,7 @@
 //     per-query max / exp2 / sum (warp per query), P.V (thread = value column
 //     pair x key part), with the running output rescaled when the maximum moves;
 //   * it writes its unnormalised partial output o, running maximum m and sum l to
-//     the workspace; a second kernel merges the ranges of each (b, h):
+//     the workspace; a second kernel merges the ranges (or chunks) of each (b, h):
 //     o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, M = max_s m_s.
 // Waits on the copy barriers are bounded in time; a wait that runs out records a
 // fault bit (attn_fault_status) and the CTA stops after its copies have landed.
@@ -76,6 +79,8 @@ struct DecodeParams {
   float* ws_o;   // [BH][splits][n_q][D]
   float* ws_ml;  // [BH][splits][n_q][2]
   int H, n_q, n_max, splits;
+  int BH;          // B * H
+  int chunk_keys;  // one query: keys per chunk (one warp each)
   float scale_log2;
 };
 
@@ -110,6 +115,214 @@ __device__ __forceinline__ void split_tiles(int len, int splits, int s, int& t0,
   const int per = (tiles + splits - 1) / splits;
   t0 = min(s * per, tiles);
   t1 = min(t0 + per, tiles);
+}
+
+// ---------------------------------------------------------------- one query
+// One query per (b, h), the usual generation step: every warp is independent. The
+// cache of each (b, h) is cut into chunks of `chunk_keys` keys, one warp each; the
+// warp streams its chunk's 32-key K and V tiles through a private ring of bulk copies
+// (its own mbarriers, no block-wide barrier anywhere) and keeps the online softmax in
+// registers. Within a tile, a K or V row of D bf16 is read by D / 8 lanes, 16 bytes
+// each (lane group = key, lane within the group = 8 value columns): a score is the
+// lane's 8-term dot product summed over its group with shuffles; the lane's 8 output
+// columns accumulate p * v over the keys of its slot, and the slots are summed once at
+// the end. The partial (o, m, l) of each chunk goes to the workspace as a split of the
+// merge kernel below.
+// One warp per CTA, so that a warp whose chunk is short or empty hands its SM slot
+// back at once; a two-tile ring keeps a CTA at 16 KB (d = 64), thirteen of them per SM.
+// (Same-box sweeps over 1-8 warps per CTA, 1-4 stages, 16-64-key tiles and 1-4 tasks
+// per resident warp: this setting was fastest on both decode workloads.)
+template <int D>
+struct WCfg {
+  static constexpr int TKW = 32;                       // keys per tile
+  static constexpr int STAGES = 2;                     // tiles in flight per warp
+  static constexpr int WARPS = 1;                      // warps per CTA
+  static constexpr int LPR = D / 8;                    // lanes per K/V row (16 bytes each)
+  static constexpr int KPL = 32 / LPR;                 // keys per warp-wide load
+  static constexpr int NL = TKW / KPL;                 // loads per lane per tile
+  static constexpr int TILE_BYTES = TKW * D * 2;
+  static constexpr int WARP_BYTES = STAGES * 2 * TILE_BYTES;  // K ring, then V ring
+  static constexpr int OFF_BAR = WARPS * WARP_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + WARPS * STAGES * 8;
+  static constexpr int MIN_CHUNK = 4 * TKW;            // at least four tiles per warp
+  static constexpr int CTAS_PER_SM = (228 * 1024) / (SMEM_BYTES + 1024);  // 1 KB reserved per CTA
+  static constexpr int TASKS_PER_WARP = 2;              // chunks per resident warp
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 r;
+  // ordered after the mbarrier wait that made the tile visible (memory clobber)
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr)
+               : "memory");
+  return r;
+}
+
+// Streams one chunk of the cache of (b, h) = bh and writes its partial (o, m, l) to
+// workspace row ws_row; false if a copy never completed (recorded as a fault).
+template <int D>
+__device__ __forceinline__ bool stream_chunk(const DecodeParams& p, int bh, int k0, int nk, size_t ws_row, int warp,
+                                             int lane) {
+  using C = WCfg<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t s_w = ptx::smem_u32(smem) + warp * C::WARP_BYTES;
+  const uint32_t bar0 = ptx::smem_u32(smem) + C::OFF_BAR + warp * C::STAGES * 8;
+  const int n_tiles = (nk + C::TKW - 1) / C::TKW;
+  const size_t row0 = (size_t)bh * p.n_max + k0;  // first cache row of the chunk
+  if (lane == 0) {
+    for (int st = 0; st < C::STAGES; ++st) ptx::mbar_init(bar0 + 8 * st, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  auto issue = [&](int it) {  // tile it of the chunk into stage it % STAGES
+    const int rows = min(C::TKW, nk - it * C::TKW);
+    const uint32_t bytes = (uint32_t)rows * D * 2;
+    const int st = it % C::STAGES;
+    const size_t off = (row0 + (size_t)it * C::TKW) * D;
+    ptx::mbar_arrive_expect_tx(bar0 + 8 * st, 2 * bytes);
+    bulk_load(s_w + st * C::TILE_BYTES, p.k + off, bytes, bar0 + 8 * st);
+    bulk_load(s_w + (C::STAGES + st) * C::TILE_BYTES, p.v + off, bytes, bar0 + 8 * st);
+  };
+  if (lane == 0)
+    for (int it = 0; it < min(C::STAGES, n_tiles); ++it) issue(it);
+
+  // this lane's 8 query columns, widened and pre-multiplied by scale * log2(e)
+  const int cg = lane % C::LPR, ks = lane / C::LPR;
+  float qf[8];
+  {
+    const uint4 qw = *reinterpret_cast<const uint4*>(p.q + (size_t)bh * D + 8 * cg);
+    const uint32_t w4[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qf[2 * e] = __uint_as_float(w4[e] << 16) * p.scale_log2;
+      qf[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u) * p.scale_log2;
+    }
+  }
+  float o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;
+
+  bool ok = true;
+  int it_fail = 0;
+  for (int it = 0; it < n_tiles; ++it) {
+    const int st = it % C::STAGES;
+    if (!__all_sync(0xffffffffu, wait_full(bar0 + 8 * st, (it / C::STAGES) & 1))) {
+      ok = false;
+      it_fail = it;
+      break;
+    }
+    const int rows = min(C::TKW, nk - it * C::TKW);
+    const uint32_t k_t = s_w + st * C::TILE_BYTES + cg * 16;
+    const uint32_t v_t = s_w + (C::STAGES + st) * C::TILE_BYTES + cg * 16;
+    // scores of the keys ks + KPL * i of this tile (log2 units)
+    float sc[C::NL];
+#pragma unroll
+    for (int i = 0; i < C::NL; ++i) {
+      const uint4 kw = lds128(k_t + (ks + C::KPL * i) * (D * 2));
+      const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+      float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        d0 = fmaf(qf[2 * e], __uint_as_float(w4[e] << 16), d0);
+        d1 = fmaf(qf[2 * e + 1], __uint_as_float(w4[e] & 0xffff0000u), d1);
+      }
+      sc[i] = d0 + d1;
+    }
+#pragma unroll
+    for (int x = 1; x < C::LPR; x <<= 1)
+#pragma unroll
+      for (int i = 0; i < C::NL; ++i) sc[i] += __shfl_xor_sync(0xffffffffu, sc[i], x);
+    float mt = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < C::NL; ++i) {
+      if (ks + C::KPL * i >= rows) sc[i] = -INFINITY;  // past the end of the cache
+      mt = fmaxf(mt, sc[i]);
+    }
+#pragma unroll
+    for (int x = C::LPR; x < 32; x <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, x));
+    const float m_new = fmaxf(m_run, mt);
+    const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+    const float alpha = ptx::ex2(m_run - m_use);  // 0 while nothing was legal
+    float pr[C::NL], ps = 0.0f;
+#pragma unroll
+    for (int i = 0; i < C::NL; ++i) {
+      pr[i] = ptx::ex2(sc[i] - m_use);
+      ps += pr[i];
+    }
+#pragma unroll
+    for (int x = C::LPR; x < 32; x <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, x);
+    l_run = l_run * alpha + ps;
+    m_run = m_new;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] *= alpha;
+#pragma unroll
+    for (int i = 0; i < C::NL; ++i) {
+      if (ks + C::KPL * i < rows) {  // rows past the end hold stale bytes
+        const uint4 vw = lds128(v_t + (ks + C::KPL * i) * (D * 2));
+        const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          o[2 * e] = fmaf(pr[i], __uint_as_float(w4[e] << 16), o[2 * e]);
+          o[2 * e + 1] = fmaf(pr[i], __uint_as_float(w4[e] & 0xffff0000u), o[2 * e + 1]);
+        }
+      }
+    }
+    __syncwarp();  // every lane has read stage st
+    if (lane == 0 && it + C::STAGES < n_tiles) issue(it + C::STAGES);
+  }
+
+  if (!ok) {
+    // a copy never completed: record it, let this warp's copies in flight land, stop
+    if (lane == 0) {
+      atomicOr(&g_decode_fault_word, FAULT_DECODE);
+      for (int it = it_fail; it < min(it_fail + C::STAGES, n_tiles); ++it) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar0 + 8 * (it % C::STAGES), (it / C::STAGES) & 1))
+          if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) break;
+      }
+    }
+    __syncwarp();
+    return false;
+  }
+  // sum the key slots; the lanes of slot 0 write the chunk's 8-column pieces
+#pragma unroll
+  for (int x = C::LPR; x < 32; x <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] += __shfl_xor_sync(0xffffffffu, o[e], x);
+  if (ks == 0) {
+    float4* dst = reinterpret_cast<float4*>(p.ws_o + ws_row * D + 8 * cg);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+  }
+  if (lane == 0) {
+    p.ws_ml[ws_row * 2 + 0] = m_run;
+    p.ws_ml[ws_row * 2 + 1] = l_run;
+  }
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(WCfg<D>::WARPS * 32) attn_decode_warp_kernel(const DecodeParams p) {
+  using C = WCfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long task = (long long)blockIdx.x * C::WARPS + warp;  // (b*h, chunk)
+  if (task >= (long long)p.BH * p.splits) return;
+  const int bh = (int)(task / p.splits), chunk = (int)(task % p.splits);
+  const int b = bh / p.H;
+  const int len = min(max(p.cache_lens[b], 0), p.n_max);
+  const int k0 = chunk * p.chunk_keys;
+  const int nk = max(0, min(len - k0, p.chunk_keys));
+  const size_t ws_row = (size_t)bh * p.splits + chunk;
+  if (nk > 0) {
+    if (!stream_chunk<D>(p, bh, k0, nk, ws_row, warp, lane)) {
+      if (lane == 0) p.ws_ml[ws_row * 2 + 1] = 0.0f;  // a failed chunk contributes nothing
+    }
+  } else if (lane == 0) {  // nothing of this (b, h) in the chunk: an empty split
+    p.ws_ml[ws_row * 2 + 0] = -INFINITY;
+    p.ws_ml[ws_row * 2 + 1] = 0.0f;
+  }
 }
 
 // NQ: compile-time bucket of the query count (n_q <= NQ), so that the per-query
@@ -345,14 +558,6 @@ __global__ void __launch_bounds__(NTHREADS) attn_decode_combine_kernel(const Dec
 template <int D>
 int launch_decode(const DecodeArgs& a, float* ws) {
   using C = DCfg<D>;
-  void (*split_kernel)(const DecodeParams) = a.n_q <= 1   ? attn_decode_split_kernel<D, 1>
-                                             : a.n_q <= 2 ? attn_decode_split_kernel<D, 2>
-                                             : a.n_q <= 4 ? attn_decode_split_kernel<D, 4>
-                                             : a.n_q <= 8 ? attn_decode_split_kernel<D, 8>
-                                                          : attn_decode_split_kernel<D, 16>;
-  if (cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-      cudaSuccess)
-    return ATTN_ERR_CUDA;
   DecodeParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.k = static_cast<const uint16_t*>(a.k);
@@ -363,14 +568,32 @@ int launch_decode(const DecodeArgs& a, float* ws) {
   p.H = a.H;
   p.n_q = a.n_q;
   p.n_max = a.n_max;
-  p.splits = decode_splits(a.B, a.H, a.n_max);
+  p.splits = decode_splits(a.B, a.H, a.n_q, a.n_max, D);
+  p.chunk_keys = decode_chunk_keys(a.B, a.H, a.n_max, D);
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   const long long bh = (long long)a.B * a.H;
   if (bh > 65535) return ATTN_ERR_UNSUPPORTED;  // one grid row per (b, h)
+  p.BH = (int)bh;
   p.ws_o = ws;
   p.ws_ml = ws + (size_t)bh * p.splits * a.n_q * D;
-  dim3 grid(p.splits, (unsigned)bh);
-  split_kernel<<<grid, NTHREADS, C::SMEM_BYTES, a.stream>>>(p);
+  if (a.n_q == 1) {
+    using W = WCfg<D>;
+    if (cudaFuncSetAttribute(attn_decode_warp_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             W::SMEM_BYTES) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    // one warp per (b*h, chunk) task, consecutive chunks of a (b, h) in one CTA
+    const unsigned blocks = (unsigned)((bh * p.splits + W::WARPS - 1) / W::WARPS);
+    attn_decode_warp_kernel<D><<<blocks, W::WARPS * 32, W::SMEM_BYTES, a.stream>>>(p);
+  } else {
+    void (*split_kernel)(const DecodeParams) = a.n_q <= 2   ? attn_decode_split_kernel<D, 2>
+                                               : a.n_q <= 4 ? attn_decode_split_kernel<D, 4>
+                                               : a.n_q <= 8 ? attn_decode_split_kernel<D, 8>
+                                                            : attn_decode_split_kernel<D, 16>;
+    if (cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    split_kernel<<<dim3(p.splits, (unsigned)bh), NTHREADS, C::SMEM_BYTES, a.stream>>>(p);
+  }
   if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   attn_decode_combine_kernel<D><<<(unsigned)bh, NTHREADS, 0, a.stream>>>(p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -378,8 +601,32 @@ int launch_decode(const DecodeArgs& a, float* ws) {
 
 }  // namespace
 
-int decode_splits(int B, int H, int n_max) {
+// One query: keys per warp task. About TASKS_PER_WARP tasks per resident warp over the
+// whole cache extent, at least MIN_CHUNK keys each, a whole number of 32-key tiles.
+template <int D>
+static long long decode_tasks_target() {
+  using W = WCfg<D>;
+  return (long long)W::TASKS_PER_WARP * 152 * W::CTAS_PER_SM * W::WARPS;
+}
+
+int decode_chunk_keys(int B, int H, int n_max, int d) {
   const long long bh = (long long)B * H;
+  const long long target = d == 64 ? decode_tasks_target<64>() : decode_tasks_target<128>();
+  const int min_chunk = d == 64 ? WCfg<64>::MIN_CHUNK : WCfg<128>::MIN_CHUNK;
+  long long per = (target + bh - 1) / bh;  // chunks per (b, h)
+  const long long most = (n_max + min_chunk - 1) / min_chunk;
+  if (per > most) per = most;
+  if (per < 1) per = 1;
+  const long long chunk = ((n_max + per - 1) / per + 31) / 32 * 32;
+  return (int)chunk;
+}
+
+int decode_splits(int B, int H, int n_q, int n_max, int d) {
+  const long long bh = (long long)B * H;
+  if (n_q == 1) {
+    const int chunk = decode_chunk_keys(B, H, n_max, d);
+    return (n_max + chunk - 1) / chunk;
+  }
   const long long target = 4LL * 152;  // CTAs to cover every SM a few times
   long long s = (target + bh - 1) / bh;
   const long long tiles = (n_max + TK - 1) / TK;
@@ -389,7 +636,7 @@ int decode_splits(int B, int H, int n_max) {
 }
 
 size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d) {
-  const size_t rows = (size_t)B * H * decode_splits(B, H, n_max) * n_q;
+  const size_t rows = (size_t)B * H * decode_splits(B, H, n_q, n_max, d) * n_q;
   return rows * ((size_t)d + 2) * sizeof(float);
 }
 

@@ -102,7 +102,8 @@ int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc);   // attn_fwd_tc.cu
 bool use_single_tile(const TcArgs& a);                      // attn_fwd_tc.cu
 int launch_attn_f32(const F32Args& a);                       // attn_fwd_f32.cu
 int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd_tc.cu
-int decode_splits(int B, int H, int n_max);                              // attn_decode.cu
+int decode_splits(int B, int H, int n_q, int n_max, int d);               // attn_decode.cu
+int decode_chunk_keys(int B, int H, int n_max, int d);                    // attn_decode.cu
 size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d);  // attn_decode.cu
 int launch_attn_decode(const DecodeArgs& a, void* workspace);            // attn_decode.cu
 int launch_attn_decode_noalloc(const DecodeArgs& a);                     // attn_decode.cu
