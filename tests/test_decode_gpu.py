@@ -68,6 +68,19 @@ def test_decode_ragged(orc, d, n_q, n_max):
     check(out, lse, ref, ref_lse)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_one_query_chunk_and_tile_edges(orc, d):
+    """One query per (b, h) runs one warp per cache chunk: for 8 heads and a 4096-key
+    cache that is 32 chunks of 128 keys in 32-key tiles. Cache lengths on and beside
+    those boundaries, a length inside the first tile, and the full cache."""
+    w = W.WORKLOADS["decode_b32_h8_q1_k2048_d64"]
+    q, k, v, _ = W.make_inputs(w, seed=5300 + d, B=8, H=1, n_q=1, n_k=4096, d_k=d, d_v=d)
+    lens = np.array([896, 897, 895, 31, 32, 33, 4096, 4095], np.int32)
+    out, lse = run_decode(q, k, v, lens, W.default_scale(d), ws_fill=0xFF)  # NaN-filled workspace
+    ref, ref_lse = orc.attention(q, k, v, W.default_scale(d), DEC, lens)
+    check(out, lse, ref, ref_lse)
+
+
 def test_decode_equals_last_rows_of_causal_forward(orc):
     """The decode step and the causal forward kernel agree on the newest positions."""
     w = W.WORKLOADS["decoder_causal_b16_h8_n512_d64"]
