@@ -11,7 +11,7 @@
 //
 // Two schedules. The deterministic one (any d, or on request) has three kernels and
 // no atomics:
-//   attn_bwd_dot_kernel   D_i = dO_i . O_i (fp32), one warp per row, written with
+//   attn_bwd_dot_kernel   D_i = dO_i . O_i (fp32), d / 8 lanes per row, written with
 //                         -lse_i log2(e) into a per-tile table the other two kernels
 //                         read (the dK/dV kernel with one bulk copy per query tile);
 //   attn_bwd_dkdv_kernel  one CTA per 128-key tile of one (b, h); it streams the
@@ -157,38 +157,58 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
 
 // ------------------------------------------------------------------ D_i = dO_i . O_i
 // Row r of the padded table (bh, tile, i): -lse_i log2(e) and -D_i, D_i = dO_i . O_i;
-// rows past n_q get -inf (so P = 0) and 0.
+// rows past n_q get -inf (so P = 0) and 0. A row of O or dO (D bf16) is read by D / 8
+// lanes, 16 bytes each, so a warp reads whole rows with coalesced 16-byte loads; each
+// warp takes DOT_STEPS groups of rows and issues all their loads before the arithmetic,
+// which keeps enough bytes in flight to stream O and dO at HBM speed.
+constexpr int DOT_STEPS = 4;
+template <int D>
+__host__ __device__ constexpr int dot_rows_per_warp() {
+  return (32 / (D / 8)) * DOT_STEPS;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const uint16_t* out, const uint16_t* dout, const float* lse,
                                                            float* stats, int n_q, int q_tiles, long long rows) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // bh * q_tiles * T + i
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const long long bh = row / ((long long)q_tiles * T);
-  const int i = (int)(row - bh * q_tiles * T);
-  float* dst = stats + (bh * q_tiles + i / T) * 2 * T + (i % T);
-  if (i >= n_q) {
-    if (lane == 0) {
-      dst[0] = -INFINITY;
-      dst[T] = 0.0f;
+  constexpr int LPR = D / 8;      // lanes per row
+  constexpr int RPS = 32 / LPR;   // rows per warp per step
+  const int lane = threadIdx.x & 31, cg = lane % LPR;
+  const long long first = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * dot_rows_per_warp<D>() + lane / LPR;
+  const long long per_bh = (long long)q_tiles * T;
+  uint4 o4[DOT_STEPS], g4[DOT_STEPS];
+  long long src[DOT_STEPS];  // row of out / dout / lse, or -1 for a padding row or none
+#pragma unroll
+  for (int u = 0; u < DOT_STEPS; ++u) {
+    const long long row = first + (long long)u * RPS;  // bh * q_tiles * T + i
+    const long long bh = row / per_bh;
+    const int i = (int)(row - bh * per_bh);
+    src[u] = (row < rows && i < n_q) ? bh * n_q + i : -1;
+    o4[u] = make_uint4(0, 0, 0, 0);
+    g4[u] = make_uint4(0, 0, 0, 0);
+    if (src[u] >= 0) {
+      o4[u] = __ldg(reinterpret_cast<const uint4*>(out + src[u] * D) + cg);
+      g4[u] = __ldg(reinterpret_cast<const uint4*>(dout + src[u] * D) + cg);
     }
-    return;
-  }
-  const long long src = bh * n_q + i;
-  const uint32_t* o = reinterpret_cast<const uint32_t*>(out + src * D);
-  const uint32_t* g = reinterpret_cast<const uint32_t*>(dout + src * D);
-  float acc = 0.0f;
-#pragma unroll
-  for (int x = lane; x < D / 2; x += 32) {
-    const uint32_t a = o[x], b = g[x];
-    acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
-    acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    dst[0] = -lse[src] * 1.4426950408889634f;
-    dst[T] = -acc;
+  for (int u = 0; u < DOT_STEPS; ++u) {
+    const uint32_t a[4] = {o4[u].x, o4[u].y, o4[u].z, o4[u].w}, b[4] = {g4[u].x, g4[u].y, g4[u].z, g4[u].w};
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(a[e] << 16), __uint_as_float(b[e] << 16), acc);
+      acc = fmaf(__uint_as_float(a[e] & 0xffff0000u), __uint_as_float(b[e] & 0xffff0000u), acc);
+    }
+#pragma unroll
+    for (int off = 1; off < LPR; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const long long row = first + (long long)u * RPS;
+    if (cg == 0 && row < rows) {
+      const long long bh = row / per_bh;
+      const int i = (int)(row - bh * per_bh);
+      float* dst = stats + (bh * q_tiles + i / T) * 2 * T + (i % T);
+      dst[0] = src[u] >= 0 ? -lse[src[u]] * 1.4426950408889634f : -INFINITY;
+      dst[T] = src[u] >= 0 ? -acc : 0.0f;
+    }
   }
 }
 
@@ -719,8 +739,9 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_ac
     return ATTN_ERR_CUDA;
   const int q_tiles = (a.n_q + T - 1) / T;
   const long long rows = (long long)BH * q_tiles * T;
-  if ((rows + 7) / 8 > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, a.stream>>>(
+  const long long rows_per_block = 8LL * dot_rows_per_warp<D>();
+  if ((rows + rows_per_block - 1) / rows_per_block > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  attn_bwd_dot_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, a.stream>>>(
       static_cast<const uint16_t*>(a.out), static_cast<const uint16_t*>(a.dout), a.lse, stats, a.n_q, q_tiles, rows);
   if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   BwdParams p;
