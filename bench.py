@@ -86,7 +86,7 @@ NCU_TRAFFIC = {
     # profiles/attn_decode_warp_kernel_decode_b16_h16_q1_k8192_d64.md (warp kernel only)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "eea7282b512de8b3"): 424485376,
     # profiles/attn_bwd_tc_kernel_long_causal_b2_h16_n8192_d64.md (the fused d = 64 kernel)
-    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "a1b730ba328d5ec0"): 1064478976,
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "fcd11ba67cb5c639"): 1059860224,
 }
 
 
