@@ -149,7 +149,6 @@ int launch_attn_host(const TcArgs& a, PFN_encodeTiled enc, void* workspace) {
       chunk_plan((long long)a.B * a.H, hb, a.n_q, a.n_k, a.d, (a.mask_mode & ATTN_MASK_CAUSAL) != 0, sizes);
   long long caps[kSlots];
   slot_caps(sizes, n_chunks, caps);
-  const bool single = use_single_tile(a);  // chosen for the whole problem, not per chunk
   uint8_t* base = static_cast<uint8_t*>(workspace);
   int32_t* d_lens = reinterpret_cast<int32_t*>(base);
   uint8_t* slot_base[kSlots] = {};
@@ -196,7 +195,6 @@ int launch_attn_host(const TcArgs& a, PFN_encodeTiled enc, void* workspace) {
       TcArgs t{sq + r * hb.q, sk + r * hb.kv, sv + r * hb.kv, so + r * hb.o,
                a.lse ? reinterpret_cast<float*>(sl + r * hb.l) : nullptr, pb, ph, a.n_q, a.n_k, a.d, a.scale,
                a.mask_mode, padding ? d_lens + b : nullptr, st.comp[s], -1};
-      t.single_tile = single ? 1 : 0;
       if ((rc = launch_attn_tc(t, enc)) != ATTN_OK) return rc;
       f += (long long)pb * ph;
     }

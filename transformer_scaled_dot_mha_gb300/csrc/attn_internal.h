@@ -29,7 +29,6 @@ struct TcArgs {
   cudaStream_t stream;
   int window;  // local-window radius (>= 0), or -1 for none
   int heads_interleaved = 0;  // 1: q, k, v, out are [B, n, H*d] instead of [B, H, n, d]
-  int single_tile = -1;       // -1: choose by the grid size; 0 / 1: force the variant (d = 64)
 };
 
 // Validated arguments of one fp32 call.
@@ -99,7 +98,6 @@ struct MhaArgs {
 };
 
 int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc);   // attn_fwd_tc.cu
-bool use_single_tile(const TcArgs& a);                      // attn_fwd_tc.cu
 int launch_attn_f32(const F32Args& a);                       // attn_fwd_f32.cu
 int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd_tc.cu
 int decode_splits(int B, int H, int n_q, int n_max, int d);               // attn_decode.cu
