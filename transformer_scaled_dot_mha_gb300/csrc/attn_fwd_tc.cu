@@ -225,7 +225,12 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
   int jb0 = 0, n_t0, jb1 = 0, n_t1;
   if constexpr (LOCAL) {
     tile_range(row0, p.n_q, kv_len, causal, window, jb0, n_t0);
-    tile_range(row0 + BM, p.n_q, kv_len, causal, window, jb1, n_t1);
+    if constexpr (SINGLE) {
+      jb1 = jb0;
+      n_t1 = 0;
+    } else {
+      tile_range(row0 + BM, p.n_q, kv_len, causal, window, jb1, n_t1);
+    }
   } else {
     const int kv_tiles = (kv_len + BN - 1) / BN;
     n_t0 = tiles_for(row0, p.n_q, kv_tiles, causal);
@@ -738,12 +743,15 @@ int launch(const TcArgs& a, PFN_encodeTiled enc) {
       encode_map(enc, &mk, a.k, D, a.n_k, a.B * a.H) != CUDA_SUCCESS ||
       encode_map(enc, &mv, a.v, D, a.n_k, a.B * a.H) != CUDA_SUCCESS)
     return ATTN_ERR_UNSUPPORTED;
-  if (a.window >= 0) return launch_variant<D, true, false>(a, mq, mk, mv);
-  // d = 64 without a window runs the one-tile variant (one 128-row Q tile per CTA, two
-  // CTAs per SM) at every size: each CTA's prologue and epilogue overlap the other
-  // CTA's softmax, which measured faster on short and long workloads alike (long causal
-  // n = 8192: 282.8 -> 266.1 us against two Q tiles per CTA). The two-tile kernel serves
-  // d = 128 (two d = 128 CTAs do not fit one SM's shared memory) and the local window.
+  if (a.window >= 0) {
+    if constexpr (D == 64) return launch_variant<D, true, false, true>(a, mq, mk, mv);
+    else return launch_variant<D, true, false>(a, mq, mk, mv);
+  }
+  // d = 64 runs the one-tile variant (one 128-row Q tile per CTA, two CTAs per SM) at
+  // every size, with or without a window: each CTA's prologue and epilogue overlap the
+  // other CTA's softmax, which measured faster on short and long workloads alike (long
+  // causal n = 8192: 282.8 -> 266.1 us against two Q tiles per CTA). The two-tile
+  // kernel serves d = 128, where two CTAs do not fit one SM's shared memory.
   if constexpr (D == 64) return launch_variant<D, false, false, true>(a, mq, mk, mv);
   else return launch_variant<D, false, false>(a, mq, mk, mv);
 }
