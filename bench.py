@@ -82,7 +82,7 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "18a644fb88b39b29"): 155990784,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "a52bd19927b92155"): 155677952,
     # profiles/attn_decode_warp_kernel_decode_b16_h16_q1_k8192_d64.md (warp kernel only)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "eea7282b512de8b3"): 424485376,
     # profiles/attn_bwd_tc_kernel_long_causal_b2_h16_n8192_d64.md (the fused d = 64 kernel)
