@@ -98,6 +98,13 @@ def test_decode_workspace_and_argument_checks(L):
     ws = attn.attn_decode_workspace_size
     assert ws(16, 16, 1, 8192, 64) > 0 and ws(16, 16, 1, 8192, 64) == ws(16, 16, 1, 8192, 64)
     assert ws(1, 1, 17, 100, 64) == 0 and ws(1, 1, 1, 100, 96) == 0 and ws(0, 1, 1, 100, 64) == 0
+    # one query: one fp32 partial (d outputs, max, sum) per cache chunk of each (b, h); the
+    # chunk count follows the resident warps, not the cache length, so it stays small
+    for B, H, n, d in ((16, 16, 8192, 64), (32, 8, 2048, 64), (3, 5, 1000, 128), (1, 1, 1 << 24, 64)):
+        nbytes = ws(B, H, 1, n, d)
+        assert nbytes > 0 and nbytes % (B * H * (d + 2) * 4) == 0
+        assert nbytes <= attn.NOALLOC_MAX_BYTES  # attn_decode_noalloc serves these shapes
+    assert ws(1, 1, 1, 1 << 24, 64) < 4096 * 66 * 4
     need = ws(2, 3, 4, 500, 128)
     f = L.attn_decode
     ok = dict(q=16, k=32, v=48, out=64, lse=None, B=2, h=3, n_q=4, n_max=500, d=128, scale=0.088,
