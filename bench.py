@@ -35,6 +35,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -82,19 +83,29 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "a52bd19927b92155"): 155677952,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "105f4faaa1b8054d"): 155677952,
     # profiles/attn_decode_warp_kernel_decode_b16_h16_q1_k8192_d64.md (warp kernel only)
-    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "eea7282b512de8b3"): 424485376,
+    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "a3b9d57c7afa8ca3"): 424485376,
     # profiles/attn_bwd_tc_kernel_long_causal_b2_h16_n8192_d64.md (the fused d = 64 kernel)
-    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "fcd11ba67cb5c639"): 1059860224,
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "f4b90b7e38fe3b46"): 1059860224,
 }
+
+
+_C_COMMENT = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(src: str) -> str:
+    """C++ source without its comments and blank lines (string literals kept): DRAM
+    traffic depends on the code, so a comment edit must not invalidate a capture."""
+    s = _C_COMMENT.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", src)
+    return "\n".join(line.rstrip() for line in s.splitlines() if line.strip())
 
 
 def kernel_source_hash(kernel: str = "attn_fwd_tc_kernel") -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "transformer_scaled_dot_mha_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "transformer_scaled_dot_mha_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

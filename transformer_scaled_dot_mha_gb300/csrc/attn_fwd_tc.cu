@@ -10,26 +10,26 @@
 // section 6.1 notes leaves the mathematics unchanged -- so the n x n score
 // matrix never leaves the SM.
 //
-// Work decomposition. One CTA owns 256 query rows of one (b, h): two 128-row Q
-// tiles. It streams 128-key K/V tiles through a shared-memory ring filled by TMA.
-// Warps 0-3 and 4-7 are the softmax warpgroups of Q tiles 0 and 1 (thread =
-// query row = TMEM lane); warp 8 is the TMA producer; warp 9 allocates and frees
-// TMEM. The control warps hand registers to the softmax warps with setmaxnreg.
+// Work decomposition. A CTA owns one or two 128-row Q tiles of one (b, h) and
+// streams 128-key K/V tiles through a shared-memory ring filled by TMA. Each Q tile
+// has a softmax warpgroup (thread = query row = TMEM lane); then come the TMA
+// producer warp and the MMA issuer warps. The control warps hand registers to the
+// softmax warps with setmaxnreg.
 //
-// Tensor memory (512 columns x 128 lanes of 32 bit), fp32 S and O, bf16-pair P:
-//   D = 64:  S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0 [384,448) O1 [448,512)
-//   D = 128: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_t overwrites the
-//            first 64 columns of S_t.
-//
-// D = 64 (512 threads): P has its own columns, so a softmax warpgroup releases
-// S_t as soon as it has loaded it. Four issuer warps -- 9 + t issues S_t, 11 + t
-// issues PV_t -- run S_t(j+1) = Q_t K_{j+1}^T while the softmax of tile j is still
-// exponentiating, and PV_t(j) during the softmax of tile j+1; the softmax waits
-// for PV_t(j-1) only before it overwrites P_t. K/V stages are released by two
-// arrivals (both Q tiles).
-// D = 128 (384 threads): P lives in S, so S_t(j) must follow PV_t(j-1). One issuer
-// (warp 9) runs, in order, PV0(j-1), S0(j), PV1(j-1), S1(j): each softmax
-// warpgroup works while the tensor core serves the other tile.
+// D = 64 runs one Q tile per CTA (template flag SINGLE), two CTAs per SM, 256
+// threads: warps 0-3 softmax, 4 producer, 5 issues S, 7 issues PV. TMEM (256 columns
+// x 128 lanes of 32 bit): S [0,128), P [128,192) (bf16 pairs), O [192,256). P has its
+// own columns, so the softmax releases S as soon as it has loaded it: S(j+1) =
+// Q K_{j+1}^T runs while the softmax of tile j is still exponentiating, and PV(j)
+// during the softmax of tile j+1; the softmax waits for PV(j-1) only before it
+// overwrites P. The two CTAs on an SM overlap each other's prologue and epilogue.
+// D = 128 runs two Q tiles per CTA, one CTA per SM, 384 threads: warps 0-3 and 4-7
+// softmax, 8 producer, 9 the one issuer. TMEM (512 columns): S0 [0,128) S1 [128,256)
+// O0 [256,384) O1 [384,512); P_t overwrites the first 64 columns of S_t, so S_t(j)
+// must follow PV_t(j-1), and the issuer runs, in order, PV0(j-1), S0(j), PV1(j-1),
+// S1(j): each softmax warpgroup works while the tensor core serves the other tile.
+// (The template also describes a two-tile D = 64 form with separate P columns and
+// four issuers; it is no longer instantiated.)
 //
 // The softmax rescales O only when a row maximum grows by more than 2^8 (a lazy
 // reference maximum); the final O / l is exact whatever reference was used.
@@ -63,9 +63,8 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when ma
 
 constexpr uint32_t FAULT_PRODUCER = 1, FAULT_MMA = 2, FAULT_SOFTMAX = 4, FAULT_EPILOGUE = 8;
 
-// SINGLE (D = 64, short sequences): one 128-row Q tile per CTA, 256 TMEM columns, a
-// two-stage ring and 8 warps, so that two CTAs share an SM; used when the two-tile
-// grid would not fill two waves of the GPU. Otherwise two Q tiles per CTA.
+// SINGLE (D = 64): one 128-row Q tile per CTA, 256 TMEM columns, a two-stage ring and
+// 8 warps, so that two CTAs share an SM. Otherwise two Q tiles per CTA.
 template <int D, bool SINGLE = false>
 struct Cfg {
   static_assert(!SINGLE || D == 64, "single-tile variant is for d = 64");
