@@ -61,3 +61,16 @@ def test_single_process_helpers():
     assert bench.shard_seed(w, 0) == w.seed
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.weak_scaling_tflops(1e12, 10, 1000.0, 1) == pytest.approx(10.0)  # 1e13 FLOP in 1 s
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The DRAM traffic the bench reports is keyed by a hash of the kernel sources; a
+    comment or blank-line edit must keep the key, any code edit must change it."""
+    import bench
+
+    code = 'int f(int x) {\n  // scale\n  return 2 * x; /* twice */\n}\nconst char* s = "// kept";\n'
+    assert bench._code_only(code) == bench._code_only(code.replace("// scale", "// doubled\n\n"))
+    assert "// kept" in bench._code_only(code)                     # a string literal is code
+    assert bench._code_only(code) != bench._code_only(code.replace("2 * x", "3 * x"))
+    for k in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_source_hash(k)) == 16
