@@ -322,7 +322,8 @@ int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void*
  * ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA. If `clear` is non-zero the record is reset.
  * `fault_code` (may be NULL) receives the raw record: bit 0 producer, bit 1 MMA
  * issuer, bit 2 softmax, bit 3 epilogue (attn_fwd), bit 4 decode copy (attn_decode),
- * bit 5 gradient kernels (attn_bwd).
+ * bit 5 gradient kernels (attn_bwd), bit 6 attn_fwd found its shared memory not
+ * 1024-byte aligned (it then writes nothing).
  */
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code);
 

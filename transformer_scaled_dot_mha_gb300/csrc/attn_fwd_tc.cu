@@ -62,6 +62,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain copies in fl
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when max grows > 2^8
 
 constexpr uint32_t FAULT_PRODUCER = 1, FAULT_MMA = 2, FAULT_SOFTMAX = 4, FAULT_EPILOGUE = 8;
+constexpr uint32_t FAULT_SMEM_ALIGN = 64;  // dynamic shared memory not 1024-byte aligned
 
 // SINGLE (D = 64): one 128-row Q tile per CTA, 256 TMEM columns, a two-stage ring and
 // 8 warps, so that two CTAs share an SM. Otherwise two Q tiles per CTA.
@@ -74,7 +75,7 @@ struct Cfg {
   static constexpr int CHUNKS = D / 64;           // 128-byte swizzle atoms per row
   static constexpr int CHUNK_BYTES = BM * 128;    // one 128-row x 64-column slab
   static constexpr int TILE_BYTES = BM * D * 2;   // one 128-row tile of Q, K or V
-  static constexpr int STAGES = SINGLE ? 2 : (D == 64) ? 4 : 2;
+  static constexpr int STAGES = SINGLE ? 3 : (D == 64) ? 4 : 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_TILES * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
@@ -94,7 +95,9 @@ struct Cfg {
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
-  static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+  // the dynamic array is declared 1024-byte aligned (the swizzled tiles need it), so no
+  // slack: two one-tile CTAs with a three-stage ring then fit one SM
+  static constexpr int SMEM_BYTES = SMEM_USED;
   static constexpr uint32_t TMEM_COLS = SINGLE ? 256 : 512;
   static constexpr bool SEP_P = (D == 64);  // P has its own TMEM columns
   // Warps: the softmax warpgroups (one per Q tile), the TMA producer, then the MMA
@@ -120,6 +123,7 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);   // V is MN-major
   static_assert(TMEM_O + Q_TILES * D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(CTAS_PER_SM * (SMEM_BYTES + 1024) <= 228 * 1024, "CTAs per SM (1 KB reserved per CTA)");
 };
 
 struct Params {
@@ -199,8 +203,12 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D, SINGLE>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((ptx::smem_u32(smem_raw) & 1023u) != 0) {  // every CTA thread takes this branch alike
+    if (threadIdx.x == 0) atomicOr(&g_fault_word, FAULT_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t s_base = ptx::smem_u32(smem);
   const uint32_t s_q = s_base + C::OFF_Q, s_k = s_base + C::OFF_K, s_v = s_base + C::OFF_V;
   auto bar = [&](int i) -> uint32_t { return s_base + C::OFF_BAR + 8u * i; };
