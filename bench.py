@@ -83,7 +83,7 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "105f4faaa1b8054d"): 155677952,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "9d293e72bec9d960"): 146398976,
     # profiles/attn_decode_warp_kernel_decode_b16_h16_q1_k8192_d64.md (warp kernel only)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "a3b9d57c7afa8ca3"): 424485376,
     # profiles/attn_bwd_tc_kernel_long_causal_b2_h16_n8192_d64.md (the fused d = 64 kernel)
