@@ -122,8 +122,8 @@ def test_back_to_back_calls_share_the_ring():
                                   "encoder_self_pad_b32_h8_n128_d64"])
 def test_full_size_workloads(name):
     """The bench's end-to-end configurations: the ramp 3, 6, 12, 6, 5 and eight equal
-    chunks of 4 heads of n = 8192 (the two-tile variant), and one chunk of 256 heads of
-    n = 128 (the single-tile variant chosen for the whole problem)."""
+    chunks of 4 heads of n = 8192, and one chunk of 256 heads of n = 128; every chunk
+    runs the kernel instantiation the whole problem runs (one Q tile per CTA at d = 64)."""
     w = W.WORKLOADS[name]
     q, k, v, kl = W.make_inputs(w)
     assert_identical(*run_both(q, k, v, kl, w.scale, w.mask_mode))
