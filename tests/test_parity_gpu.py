@@ -228,7 +228,9 @@ def _sample_rows(B, H, n):
 
 
 @pytest.mark.parametrize("name", ["long_causal_b2_h16_n8192_d64", "long_none_b2_h16_n8192_d64",
-                                  "long_causal_b2_h16_n8192_d128", "long_none_b2_h16_n8192_d128"])
+                                  "long_causal_b2_h16_n8192_d128", "long_none_b2_h16_n8192_d128",
+                                  "long_cross_pad_b2_h16_q4096_k8192_d64",
+                                  "long_cross_pad_b2_h16_q4096_k8192_d128"])
 def test_bf16_long_sequence_sampled_rows(orc, name):
     """n = 8192 at full size: sampled rows (tile edges, ends, every 97th row of three
     heads) against the oracle, plus properties that hold for every row: each output
@@ -244,3 +246,17 @@ def test_bf16_long_sequence_sampled_rows(orc, name):
     slack = 1e-2
     assert np.all(out >= vmin - slack) and np.all(out <= vmax + slack)
     assert np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("lens", [(8192, 6145), (6144, 8191), (8064, 8065)])
+def test_bf16_long_cross_key_length_edges(orc, d, lens):
+    """Encoder-decoder attention at full size (4096 queries x 8192 keys) with key
+    lengths on, just past and just before a 128-key tile edge: sampled rows of every
+    head class against the oracle."""
+    w, (q, k, v, _) = gen(f"long_cross_pad_b2_h16_q4096_k8192_d{d}")
+    kl = np.array(lens, np.int32)
+    out, lse = run_bf16(q, k, v, kl, w.scale, P)
+    ids = _sample_rows(w.B, w.H, w.n_q)
+    ref, ref_lse = orc.attention_rows(q, k, v, w.scale, ids, P, kl)
+    assert_bf16_close(out.reshape(-1, w.d_v)[ids], lse.reshape(-1)[ids], ref, ref_lse)

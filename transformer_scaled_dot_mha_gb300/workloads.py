@@ -141,6 +141,12 @@ WORKLOADS = {w.name: w for w in [
     # restricted self-attention: each position attends to a causal neighbourhood of 512
     _wl(10, "local_causal_b2_h16_n8192_d64_w511", 2, 16, 8192, 8192, 64, "bf16", MASK_CAUSAL | MASK_WINDOW, None,
         0.5, 511),
+    # encoder-decoder attention at long lengths: 4096 decoder queries against 8192
+    # encoder keys/values with right padding (the third use of attention, n_q != n_k)
+    _wl(11, "long_cross_pad_b2_h16_q4096_k8192_d64", 2, 16, 4096, 8192, 64, "bf16", MASK_KEY_PADDING, (6144, 8192),
+        0.5),
+    _wl(12, "long_cross_pad_b2_h16_q4096_k8192_d128", 2, 16, 4096, 8192, 128, "bf16", MASK_KEY_PADDING,
+        (6144, 8192), 0.5),
 ]}
 
 
