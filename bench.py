@@ -11,8 +11,9 @@ lse stores). FLOPs are algorithmic: 2 (d_k + d_v) per legal query-key pair.
                   [--impl ours|reference] [--no-cpu-baseline] [--grad]
 
 --mha times the whole multi-head attention layer instead (one attn_mha_fwd call per
-step: the Q, K, V projections, the attention on the projections' [B, n, h*d] layout
-and the output projection; d_model = h*d, random weights resident on the device);
+step: the Q, K, V projections in one launch, the attention on the projections'
+[B, n, h*d] layout and the output projection; d_model = h*d, random weights resident
+on the device);
 FLOPs are algorithmic: 2 d_model h d per projected row for each of the four
 projections plus the attention's.
 
@@ -82,11 +83,10 @@ KERNEL_SOURCES = {
     "attn_bwd_tc_kernel": ("attn_bwd.cu", "ptx_sm103.cuh"),
 }
 NCU_TRAFFIC = {
-    # profiles/attn_fwd_tc_kernel_long_causal_b2_h16_n8192_d64.md
     ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "9d293e72bec9d960"): 146398976,
-    # profiles/attn_decode_warp_kernel_decode_b16_h16_q1_k8192_d64.md (warp kernel only)
+    # the warp kernel only (the merge kernel is not counted)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "a3b9d57c7afa8ca3"): 424485376,
-    # profiles/attn_bwd_tc_kernel_long_causal_b2_h16_n8192_d64.md (the fused d = 64 kernel)
+    # the fused d = 64 kernel
     ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "f4b90b7e38fe3b46"): 1059860224,
 }
 
@@ -751,7 +751,8 @@ def run_ours_mha(args, w):
     achieved = flops_step / (ms_per_step / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": float(peaks["bf16_tflops"]),
             "unit": "TFLOP/s", "peak_source": f"bf16_tflops (burst) of {peak_src}",
-            "kernel": "attn_mha_fwd (four cuBLASLt GEMMs + the attention kernel, timed together)", "traffic": None}
+            "kernel": ("attn_mha_fwd (the Q/K/V projection launch, the attention kernel and the output "
+                       "projection launch, timed together)"), "traffic": None}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     line = {
         "metric": "multi-head attention layer TFLOP/s on 1 GB300 and % of dense bf16 tensor peak",
@@ -765,7 +766,7 @@ def run_ours_mha(args, w):
                                 "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": args.steps * 5,
+        "gpu_launches": args.steps * 3,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
     }

@@ -23,9 +23,9 @@
  *     split_heads reshape produces, csdn blog reimplementation):
  *       q   [B, h, n_q, d_k]    k [B, h, n_k, d_k]    v [B, h, n_k, d_v]
  *       out [B, h, n_q, d_v]    lse [B, h, n_q] (float32, optional)
- *   - Every pointer is a DEVICE pointer owned by the caller. The library's own
- *     kernels allocate no device memory (attn_mha_fwd's GEMMs run on cuBLASLt, whose
- *     handle it creates once per device); it neither keeps nor frees the pointers.
+ *   - Every pointer is a DEVICE pointer owned by the caller (the *_host entry points
+ *     excepted). The library allocates no device memory; it neither keeps nor frees
+ *     the pointers.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL
  *     for the legacy default stream) and return before the GPU work finishes.
  *   - scale is used exactly as given; callers normally pass 1/sqrt(d_k) computed
@@ -178,21 +178,24 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
 /*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device memory.
  * (An addition of this library; the paper has no counterpart.)
- * Some callers have no way to obtain device scratch: code running while its stream
- * is being captured into a CUDA graph (an allocation is not a stream operation and
- * may synchronise the device or be refused during capture), latency-critical
- * serving loops that must not enter the allocator, and plug-ins whose host
- * framework owns every device buffer. This entry point takes the same arguments as
- * attn_decode minus the workspace and allocates nothing: no cudaMalloc, cudaFree or
- * allocating library call. Its scratch is a static buffer of
- * ATTN_DECODE_NOALLOC_MAX_BYTES inside the library's device image, present on every
- * GPU that loads the library until the process exits.
+ * Some callers have no way to obtain device scratch: plug-ins whose host framework
+ * owns every device buffer and hands a kernel only its inputs and outputs,
+ * latency-critical serving loops that must not enter the allocator (cudaMalloc and
+ * cudaFree can synchronise the whole device), and programs that fix their device
+ * memory at start-up. This entry point takes the same arguments as attn_decode minus
+ * the workspace and allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library call. Its scratch is a static buffer of ATTN_DECODE_NOALLOC_MAX_BYTES
+ * inside the library's device image, present on every GPU that loads the library
+ * until the process exits.
  *   - The first call on a device looks up the buffer's device address (with that
- *     device current); make that first call before any stream capture.
+ *     device current) and keeps it; make that first call before any stream capture.
+ *     A cudaDeviceReset after that first call is not supported: the kept address
+ *     belongs to the context the reset destroyed.
  *   - Every call on a device shares the one buffer, which keeps the last call's
- *     contents (the kernels write every slot before reading it, so nothing needs
- *     clearing). Calls whose GPU work overlaps -- on different streams, or from
- *     several host threads -- race on it: order them, e.g. on one stream.
+ *     contents (the kernels write every slot before reading it, an abandoned range
+ *     included, so nothing needs clearing). Calls whose GPU work overlaps -- on
+ *     different streams, or from several host threads -- race on it: order them,
+ *     e.g. on one stream.
  *   - A shape whose workspace (attn_decode_workspace_size) exceeds
  *     ATTN_DECODE_NOALLOC_MAX_BYTES returns ATTN_ERR_UNSUPPORTED and launches
  *     nothing; use attn_decode with a caller workspace for it.
@@ -277,9 +280,26 @@ int attn_bwd_host(const void* q, const void* k, const void* v, const void* out, 
                   void* stream);
 
 /*
+ * attn_linear -- one linear projection of the multi-head layer, bf16 in and out:
+ *   y[M, N] = x[M, K] w[K, N] + bias[N]
+ * The layer projects queries, keys and values with per-head matrices W_i^Q, W_i^K,
+ * W_i^V and the concatenated heads with W^O (vlmlib.cn paper summary, "multi-head
+ * attention"; the csdn blog's MultiHeadAttention uses nn.Linear layers with biases);
+ * placing the h per-head matrices side by side makes each projection this product.
+ *   x  [M, K], w [K, N] (the paper's x W orientation; an nn.Linear weight is the
+ *      transpose), y [M, N]: row-major bf16, 16-byte aligned, caller-owned device memory
+ *   bias [N] bf16, 16-byte aligned, or NULL for none.
+ * Supported: N and K multiples of 8 (16-byte rows); otherwise ATTN_ERR_UNSUPPORTED.
+ * Numerics: the products accumulate in fp32 on the sm_103a tensor cores (tcgen05,
+ * operands staged by TMA); the bias is added in fp32 and the sum rounded to bf16
+ * (nearest-even) once. One launch on `stream`; x and y must not overlap.
+ */
+int attn_linear(const void* x, const void* w, const void* bias, void* y, int M, int N, int K, void* stream);
+
+/*
  * attn_mha_workspace_size -- bytes of device workspace attn_mha_fwd needs: the
- * projected Q', K', V' and the concatenated heads (bf16) plus 32 MiB of GEMM
- * workspace. Returns 0 for an invalid or unsupported shape.
+ * projected Q', K', V' and the concatenated heads (bf16, each padded to 256 bytes).
+ * Returns 0 for an invalid or unsupported shape.
  */
 size_t attn_mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d);
 
@@ -302,12 +322,11 @@ size_t attn_mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int 
  *           aligned, owned by the caller, contents undefined on return; concurrent
  *           calls must not share it.
  * Supported: d_k == d_v in {64, 128}, d_model a multiple of 8; every pointer 16-byte
- * aligned. The four projections run on cuBLASLt (bf16 GEMMs, fp32 accumulation,
- * bias in the GEMM epilogue, results rounded to bf16); the attention is the attn_fwd
- * kernel reading Q', K', V' and writing A in their [B, n, h*d] layout, so splitting
- * and concatenating the heads moves no data. The first call on a device creates a
- * cuBLASLt handle and, for each new shape, a GEMM plan (host-side, cached). Five
- * launches on `stream`.
+ * aligned. The four projections have the numerics of attn_linear (fp32 accumulation
+ * on the tensor cores, bias added in fp32, one rounding to bf16); the three input
+ * projections run as one launch of the projection kernel. The attention is the
+ * attn_fwd kernel reading Q', K', V' and writing A in their [B, n, h*d] layout, so
+ * splitting and concatenating the heads moves no data. Three launches on `stream`.
  */
 int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void* b_q, const void* w_k,
                  const void* b_k, const void* w_v, const void* b_v, const void* w_o, const void* b_o, void* out,
@@ -323,7 +342,8 @@ int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void*
  * `fault_code` (may be NULL) receives the raw record: bit 0 producer, bit 1 MMA
  * issuer, bit 2 softmax, bit 3 epilogue (attn_fwd), bit 4 decode copy (attn_decode),
  * bit 5 gradient kernels (attn_bwd), bit 6 attn_fwd found its shared memory not
- * 1024-byte aligned (it then writes nothing).
+ * 1024-byte aligned (it then writes nothing), bit 7 projection kernel (attn_linear,
+ * attn_mha_fwd).
  */
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code);
 

@@ -63,8 +63,9 @@ class Oracle:
         self.lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, i, vp, vp, vp, i]
         self.lib.oracle_mha.argtypes = [vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, d, i, vp, vp,
                                         i]
+        self.lib.oracle_linear.argtypes = [vp, vp, vp, i, i, i, i, vp]
         for f in (self.lib.oracle_attn, self.lib.oracle_attn_rows, self.lib.oracle_attn_weights,
-                  self.lib.oracle_attn_bwd, self.lib.oracle_mha):
+                  self.lib.oracle_attn_bwd, self.lib.oracle_mha, self.lib.oracle_linear):
             f.restype = ctypes.c_int
 
     @staticmethod
@@ -190,6 +191,25 @@ class Oracle:
                                  ptr(kl), y.ctypes.data, self._threads(n_threads))
         if rc != 0:
             raise ValueError("oracle_mha rejected its arguments")
+        return y
+
+    def linear(self, x, w, b=None):
+        """One projection ``y [M, N] = x [M, K] w [K, N] + b [N]`` in float64
+        (``oracle_linear``); x, w and b share one dtype (float64, float32 or bf16 bits)."""
+        x, w = np.ascontiguousarray(x), np.ascontiguousarray(w)
+        b = None if b is None else np.ascontiguousarray(b)
+        dt = x.dtype
+        if w.dtype != dt or (b is not None and b.dtype != dt) or dt not in _DTYPES:
+            raise TypeError("x, w and b must share one of float64/float32/uint16(bf16)")
+        M, K = x.shape
+        N = w.shape[1]
+        if w.shape != (K, N) or (b is not None and b.shape != (N,)):
+            raise ValueError("shapes must be x [M, K], w [K, N], b [N]")
+        y = np.empty((M, N), np.float64)
+        rc = self.lib.oracle_linear(x.ctypes.data, w.ctypes.data, None if b is None else b.ctypes.data, _DTYPES[dt],
+                                    M, N, K, y.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_linear rejected its arguments")
         return y
 
     @staticmethod

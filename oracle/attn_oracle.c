@@ -362,3 +362,15 @@ int oracle_mha(const void* x_q, const void* x_kv, int dtype, const void* w_q, co
   free(oh);
   return rc;
 }
+
+int oracle_linear(const void* x, const void* w, const void* bias, int dtype, int M, int N, int K, double* y) {
+  if (!x || !w || !y || M <= 0 || N <= 0 || K <= 0) return -1;
+  if (dtype < ORACLE_F64 || dtype > ORACLE_BF16) return -1;
+  for (int m = 0; m < M; ++m)
+    for (int n = 0; n < N; ++n) {
+      double acc = bias ? elem(bias, dtype, n) : 0.0;
+      for (int k = 0; k < K; ++k) acc += elem(x, dtype, (long long)m * K + k) * elem(w, dtype, (long long)k * N + n);
+      y[(long long)m * N + n] = acc;
+    }
+  return 0;
+}

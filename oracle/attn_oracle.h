@@ -100,6 +100,14 @@ int oracle_mha(const void* x_q, const void* x_kv, int dtype, const void* w_q, co
                int d_k, int d_v, double scale, int mask_mode, const int* key_lens, double* y,
                int n_threads);
 
+/* One linear projection of the multi-head layer (vlmlib.cn "multi-head attention":
+ * the per-head matrices W_i side by side, x W; the csdn blog's nn.Linear with its
+ * bias): y[m, n] = bias[n] + sum_k x[m, k] w[k, n], x [M, K] and w [K, N] row-major
+ * in the paper's x W orientation, bias [N] or NULL, every input of one dtype, y
+ * [M, N] doubles accumulated in fp64 with no intermediate rounding. Returns 0, or -1
+ * on an invalid argument. */
+int oracle_linear(const void* x, const void* w, const void* bias, int dtype, int M, int N, int K, double* y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -549,4 +549,51 @@ def pin_mha_bf16_inputs_widen_exactly(orc):
     assert np.array_equal(y16, y64)
 
 
+# ---------------------------------------------------------------- linear projection
+def pin_linear_brute_force(orc):
+    """y = b + x W entry by entry: an exactly rounded sum (math.fsum) of the products
+    x[m, k] W[k, n] and the bias, on small non-square shapes (so a transposed or
+    mis-strided operand cannot pass), with and without the bias."""
+    rng = np.random.Generator(np.random.PCG64(70))
+    M, N, K = 5, 3, 7
+    x, w, b = rng.standard_normal((M, K)), rng.standard_normal((K, N)), rng.standard_normal(N)
+    for bias in (b, None):
+        y = orc.linear(x, w, bias)
+        for m in range(M):
+            for n in range(N):
+                terms = [x[m, k] * w[k, n] for k in range(K)] + ([bias[n]] if bias is not None else [])
+                assert abs(y[m, n] - math.fsum(terms)) < 1e-13
+
+
+def pin_linear_closed_forms(orc):
+    """Closed forms: x I = x exactly; a permutation matrix moves columns (x P)[:, j] =
+    x[:, p(j)]; a zero input returns the bias in every row; a projection of one row
+    with a one-hot weight column picks one input feature."""
+    rng = np.random.Generator(np.random.PCG64(71))
+    x = rng.standard_normal((4, 6))
+    assert np.array_equal(orc.linear(x, np.eye(6)), x)
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    P = np.zeros((6, 6))
+    P[perm, np.arange(6)] = 1.0
+    assert np.array_equal(orc.linear(x, P), x[:, perm])
+    b = rng.standard_normal(6)
+    assert np.array_equal(orc.linear(np.zeros((3, 6)), P, b), np.broadcast_to(b, (3, 6)))
+    e = np.zeros((6, 2))
+    e[4, 1] = 1.0
+    assert np.array_equal(orc.linear(x, e)[:, 1], x[:, 4]) and np.all(orc.linear(x, e)[:, 0] == 0.0)
+
+
+def pin_linear_matches_mha_projection(orc):
+    """The multi-head oracle's projections are this product: with one head of width
+    d_model, identity W^K = W^V = W^O, no output bias and causal masking, output
+    row 0 is x_0 W^V + b_V (it attends to itself alone) = linear(x, W^V, b_V) row 0."""
+    rng = np.random.Generator(np.random.PCG64(72))
+    d_model = 6
+    x = rng.standard_normal((1, 4, d_model))
+    wv, bv = rng.standard_normal((d_model, d_model)), rng.standard_normal(d_model)
+    eye = np.eye(d_model)
+    y = orc.mha(x, x, eye, eye, wv, eye, 1, 0.3, C, None, b_v=bv)
+    assert np.abs(y[0, 0] - orc.linear(x[0], wv, bv)[0]).max() < 1e-13
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

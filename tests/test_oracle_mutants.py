@@ -53,6 +53,10 @@ MUTANTS = {
     "mha_output_bias_dropped": ("double acc = b_o ? elem(b_o, dtype, c) : 0.0;", "double acc = 0.0;"),
     "mha_w_o_transposed": ("elem(w_o, dtype, ((long long)h * d_v + t) * d_model + c)",
                            "elem(w_o, dtype, (long long)c * H * d_v + (long long)h * d_v + t)"),
+    # linear projection
+    "linear_w_transposed": ("elem(w, dtype, (long long)k * N + n)", "elem(w, dtype, (long long)n * K + k)"),
+    "linear_bias_dropped": ("double acc = bias ? elem(bias, dtype, n) : 0.0;", "double acc = 0.0;"),
+    "linear_x_row_stride": ("elem(x, dtype, (long long)m * K + k)", "elem(x, dtype, (long long)m * N + k)"),
     "mha_concat_batch_head_swapped": ("oh[(((long long)b * H + h) * n_q + i) * d_v + t]",
                                       "oh[(((long long)h * B + b) * n_q + i) * d_v + t]"),
 }

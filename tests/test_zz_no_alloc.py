@@ -1,12 +1,14 @@
 """attn_decode_noalloc: the decode step for callers that cannot allocate device memory.
 
-Callers capturing a CUDA graph, latency-critical serving loops and plug-ins whose
-framework owns all device buffers cannot hand attn_decode a workspace. This entry
-point uses a static scratch buffer inside the library instead. The test calls it
-through the C ABI twice in a row, on different inputs, and checks each result
-against the workspace-taking attn_decode on the same inputs, within the decode
-tolerances (max |err| <= 1e-2, mean |err| <= 1e-3, lse |err| <= 1e-3); it also
-checks that a shape needing more scratch than the static buffer is refused.
+Plug-ins whose framework owns every device buffer, serving loops that must not enter
+the allocator, and programs whose device memory is fixed at start-up cannot hand
+attn_decode a workspace. This entry point uses a static scratch buffer inside the
+library instead. The test calls it through the C ABI twice in a row, on different
+inputs, and checks each result against the workspace-taking attn_decode on the same
+inputs: within the decode tolerances (max |err| <= 1e-2, mean |err| <= 1e-3, lse
+|err| <= 1e-3), and bit for bit, since both run the same kernels on the same data.
+It checks that a call after the first one leaves the device's free memory unchanged,
+and that a shape needing more scratch than the static buffer is refused.
 """
 import numpy as np
 import pytest
@@ -40,8 +42,26 @@ def test_noalloc_matches_decode_on_two_calls():
         fin = torch.isfinite(ref_lse)
         assert torch.equal(fin, torch.isfinite(lse))
         assert (lse[fin] - ref_lse[fin]).abs().max().item() <= 1e-3
+        # the same kernels on the same inputs: identical bits
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
     st, code = attn.attn_fault_status()
     assert st == attn.ATTN_OK, f"kernel fault record {code:#x}"
+
+
+def test_noalloc_call_leaves_free_memory_unchanged():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = W.WORKLOADS["decode_b32_h8_q1_k2048_d64"]
+    q, k, v, lens = W.make_inputs(w, seed=7100, B=2, H=4, n_q=2, n_k=700)
+    qd, kd, vd, ld = _dev_bf16(q), _dev_bf16(k), _dev_bf16(v), torch.from_numpy(lens).cuda()
+    out, lse = torch.empty_like(qd), torch.empty((2, 4, 2), device="cuda")
+    attn.attn_decode_noalloc(qd, kd, vd, out, ld, lse, w.scale)  # first call: loads kernels, looks up the buffer
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    attn.attn_decode_noalloc(qd, kd, vd, out, ld, lse, w.scale)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
 
 
 def test_noalloc_refuses_shapes_beyond_its_buffer():

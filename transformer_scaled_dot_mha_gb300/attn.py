@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp,
                                     ctypes.c_size_t, vp]
         L.attn_bwd_host.restype = i
+        L.attn_linear.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+        L.attn_linear.restype = i
         L.attn_mha_workspace_size.argtypes = [i, i, i, i, i, i]
         L.attn_mha_workspace_size.restype = ctypes.c_size_t
         L.attn_mha_fwd.argtypes = [vp] * 11 + [i, i, i, i, i, i, i, f, i, vp, vp, ctypes.c_size_t, vp]
@@ -71,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fault_status.restype = i
         L.attn_status_string.argtypes = [i]
         L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_internal_arm_wait_timeout.argtypes = [ctypes.c_ulonglong, i]
+        L.attn_internal_arm_wait_timeout.restype = None
         _lib = L
     return _lib
 
@@ -357,6 +361,31 @@ def attn_mha_fwd(x_q, x_kv, w_q, w_k, w_v, w_o, out, H, workspace, b_q=None, b_k
     if st != ATTN_OK:
         raise AttnError(st, "attn_mha_fwd")
     return out
+
+
+def attn_linear(x, w, y, bias=None, stream=None):
+    """One projection ``y [M, N] = x [M, K] w [K, N] + bias [N]`` (bf16, row-major,
+    caller-provided ``y``)."""
+    _check(x, "x", torch.bfloat16, 2)
+    _check(w, "w", torch.bfloat16, 2)
+    _check(y, "y", torch.bfloat16, 2)
+    if bias is not None:
+        _check(bias, "bias", torch.bfloat16, 1)
+    M, K = x.shape
+    N = w.shape[1]
+    if w.shape != (K, N) or y.shape != (M, N) or (bias is not None and bias.shape != (N,)):
+        raise ValueError(f"shape mismatch: x{tuple(x.shape)} w{tuple(w.shape)} y{tuple(y.shape)}")
+    st = lib().attn_linear(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), M, N, K, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_linear")
+    return y
+
+
+def _internal_arm_wait_timeout(wait_ns: int, skip_v_tile: int) -> None:
+    """Test hook (not part of the C ABI header): the next plain d = 64 forward launch
+    made on this host thread gives up its waits after ``wait_ns`` and never copies the
+    V tile of K/V tile ``skip_v_tile``, so it ends through the bounded-wait abort path."""
+    lib().attn_internal_arm_wait_timeout(int(wait_ns), int(skip_v_tile))
 
 
 def attn_fault_status(stream=None, clear=True):

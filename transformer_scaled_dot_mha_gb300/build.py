@@ -64,7 +64,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, log in results:
             print(log)
     tmp = LIB + ".tmp"
-    cmd = [exe, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results] + ["-lcublasLt"]
+    cmd = [exe, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")

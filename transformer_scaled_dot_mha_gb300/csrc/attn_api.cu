@@ -201,9 +201,22 @@ int attn_bwd_host(const void* q, const void* k, const void* v, const void* out, 
   return attn::launch_attn_bwd_host(a, enc, workspace);
 }
 
+int attn_linear(const void* x, const void* w, const void* bias, void* y, int M, int N, int K, void* stream) {
+  if (!x || !w || !y) return ATTN_ERR_INVALID;
+  if (M <= 0 || N <= 0 || K <= 0) return ATTN_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || (bias && !aligned(bias, 16))) return ATTN_ERR_INVALID;
+  if (N % 8 != 0 || K % 8 != 0) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)M * (N > K ? N : K) > (1LL << 40) || (long long)K * N > (1LL << 40)) return ATTN_ERR_INVALID;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  const attn::LinearJob job{x, w, bias, y, M, N, K};
+  return attn::launch_linear(&job, 1, enc, static_cast<cudaStream_t>(stream));
+}
+
 size_t attn_mha_workspace_size(int B, int n_q, int n_k, int d_model, int h, int d) {
   if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || (d != 64 && d != 128)) return 0;
   if ((long long)B * (n_q > n_k ? n_q : n_k) * h * d > (1LL << 38)) return 0;
+  if ((long long)B * (n_q > n_k ? n_q : n_k) > 0x7fffffffLL) return 0;
   return attn::mha_workspace_bytes(B, n_q, n_k, h, d);
 }
 
@@ -232,12 +245,26 @@ int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void*
 }
 
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code) {
-  uint32_t w = 0, wb = 0;
+  uint32_t w = 0, wb = 0, wl = 0;
   const int st = attn::read_fault_word(static_cast<cudaStream_t>(stream), clear, &w);
-  if (st == ATTN_ERR_CUDA || attn::read_bwd_fault_word(clear, &wb) != ATTN_OK) return ATTN_ERR_CUDA;
-  w |= wb;
+  if (st == ATTN_ERR_CUDA || attn::read_bwd_fault_word(clear, &wb) != ATTN_OK ||
+      attn::read_linear_fault_word(clear, &wl) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  w |= wb | wl;
   if (fault_code) *fault_code = w;
   return w ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+// Internal test hook, deliberately not declared in attn_gb300.h: the next plain d = 64
+// attn_fwd call made on this host thread runs the fault-injection instantiation of the
+// forward kernel, whose waits give up after wait_ns and whose producer never copies
+// the V tile of K/V tile skip_v_tile. That call then ends through the bounded-wait
+// abort path and attn_fault_status reports ATTN_ERR_TIMEOUT. wait_ns is clamped to
+// [1 us, 1 s].
+void attn_internal_arm_wait_timeout(unsigned long long wait_ns, int skip_v_tile) {
+  if (wait_ns < 1000ull) wait_ns = 1000ull;
+  if (wait_ns > 1000000000ull) wait_ns = 1000000000ull;
+  attn::arm_wait_timeout_injection(wait_ns, skip_v_tile < 0 ? 0 : skip_v_tile);
 }
 
 const char* attn_status_string(int status) {

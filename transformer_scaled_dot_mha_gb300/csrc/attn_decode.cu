@@ -497,6 +497,13 @@ __global__ void __launch_bounds__(NTHREADS) attn_decode_split_kernel(const Decod
           if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) break;
       }
     }
+    // publish an empty partial (l = 0) for every query of this range, so that the
+    // merge skips it instead of reading whatever the workspace held before
+    const size_t ws_row_f = ((size_t)bh * p.splits + split) * n_q;
+    for (int q = tid; q < n_q; q += NTHREADS) {
+      p.ws_ml[(ws_row_f + q) * 2 + 0] = -INFINITY;
+      p.ws_ml[(ws_row_f + q) * 2 + 1] = 0.0f;
+    }
     __syncthreads();
     return;
   }

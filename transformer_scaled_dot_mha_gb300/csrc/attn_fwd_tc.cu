@@ -28,8 +28,6 @@
 // O0 [256,384) O1 [384,512); P_t overwrites the first 64 columns of S_t, so S_t(j)
 // must follow PV_t(j-1), and the issuer runs, in order, PV0(j-1), S0(j), PV1(j-1),
 // S1(j): each softmax warpgroup works while the tensor core serves the other tile.
-// (The template also describes a two-tile D = 64 form with separate P columns and
-// four issuers; it is no longer instantiated.)
 //
 // The softmax rescales O only when a row maximum grows by more than 2^8 (a lazy
 // reference maximum); the final O / l is exact whatever reference was used.
@@ -64,18 +62,19 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when ma
 constexpr uint32_t FAULT_PRODUCER = 1, FAULT_MMA = 2, FAULT_SOFTMAX = 4, FAULT_EPILOGUE = 8;
 constexpr uint32_t FAULT_SMEM_ALIGN = 64;  // dynamic shared memory not 1024-byte aligned
 
-// SINGLE (D = 64): one 128-row Q tile per CTA, 256 TMEM columns, a two-stage ring and
-// 8 warps, so that two CTAs share an SM. Otherwise two Q tiles per CTA.
+// SINGLE (D = 64): one 128-row Q tile per CTA, 256 TMEM columns, a three-stage ring
+// and 8 warps, so that two CTAs share an SM; P has its own TMEM columns. Otherwise
+// (D = 128) two Q tiles per CTA, one CTA per SM, P written over its S tile.
 template <int D, bool SINGLE = false>
 struct Cfg {
-  static_assert(!SINGLE || D == 64, "single-tile variant is for d = 64");
+  static_assert(SINGLE == (D == 64), "d = 64 runs one Q tile per CTA, d = 128 two");
   static constexpr int Q_TILES = SINGLE ? 1 : 2;  // Q tiles per CTA
   static constexpr int ROWS = Q_TILES * BM;       // query rows per CTA
   static constexpr int CTAS_PER_SM = SINGLE ? 2 : 1;
   static constexpr int CHUNKS = D / 64;           // 128-byte swizzle atoms per row
   static constexpr int CHUNK_BYTES = BM * 128;    // one 128-row x 64-column slab
   static constexpr int TILE_BYTES = BM * D * 2;   // one 128-row tile of Q, K or V
-  static constexpr int STAGES = SINGLE ? 3 : (D == 64) ? 4 : 2;
+  static constexpr int STAGES = SINGLE ? 3 : 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_TILES * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
@@ -87,7 +86,7 @@ struct Cfg {
   static constexpr int B_VFULL = B_KEMPTY + STAGES;
   static constexpr int B_VEMPTY = B_VFULL + STAGES;
   static constexpr int B_SFULL = B_VEMPTY + STAGES;  // [2] S_t computed
-  static constexpr int B_SFREE = B_SFULL + 2;        // [2] S_t loaded by the softmax (SEP_P only)
+  static constexpr int B_SFREE = B_SFULL + 2;        // [2] S_t loaded by the softmax (SINGLE only)
   static constexpr int B_PFULL = B_SFREE + 2;        // [2] P_t stored
   static constexpr int B_ODONE = B_PFULL + 2;        // [2] PV_t completed
   static constexpr int B_DRAIN = B_ODONE + 2;        // [4] MMA drain after an abort, one per issuer
@@ -99,26 +98,27 @@ struct Cfg {
   // slack: two one-tile CTAs with a three-stage ring then fit one SM
   static constexpr int SMEM_BYTES = SMEM_USED;
   static constexpr uint32_t TMEM_COLS = SINGLE ? 256 : 512;
-  static constexpr bool SEP_P = (D == 64);  // P has its own TMEM columns
   // Warps: the softmax warpgroups (one per Q tile), the TMA producer, then the MMA
-  // issuers -- with SEP_P four roles (S and PV per Q tile, roles 0-1 and 2-3), else one.
-  // SEP_P: 16 warps (8 with SINGLE, where roles 0-2 exist and role 1 has no tile);
-  // else 12. Register split (setmaxnreg): control warps give registers to the softmax
-  // warps; the total stays equal to the launch allocation.
+  // issuers. SINGLE: 8 warps, role 0 (warp 5) issues S, role 2 (warp 7) issues PV,
+  // warp 6 idles. Otherwise 12 warps and one issuer (warp 9). Register split
+  // (setmaxnreg): control warps give registers to the softmax warps; the total stays
+  // equal to the launch allocation.
   static constexpr int SOFTMAX_WARPS = 4 * Q_TILES;
   static constexpr int SOFTMAX_THREADS = 32 * SOFTMAX_WARPS;
   static constexpr int WARP_LOAD = SOFTMAX_WARPS;
-  static constexpr int WARP_MMA0 = SOFTMAX_WARPS + 1;  // MMA issuer role 0 (S of Q tile 0)
-  static constexpr int THREADS = SINGLE ? 256 : SEP_P ? 512 : 384;
+  static constexpr int WARP_MMA0 = SOFTMAX_WARPS + 1;  // MMA issuer role 0
+  static constexpr int THREADS = SINGLE ? 256 : 384;
   // d = 128: 72 registers keep the single MMA issuer's loop free of spills
-  static constexpr int REGS_CONTROL = SEP_P ? 40 : 72;
+  static constexpr int REGS_CONTROL = SINGLE ? 40 : 72;
   static constexpr int REGS_SOFTMAX = 216;
   static constexpr int LAUNCH_REGS = (65536 / (THREADS * CTAS_PER_SM)) & ~7;  // 128 or 168 per thread
   static_assert((THREADS - SOFTMAX_THREADS) * REGS_CONTROL + SOFTMAX_THREADS * REGS_SOFTMAX == THREADS * LAUNCH_REGS,
                 "register split");
-  static constexpr uint32_t TMEM_P = SINGLE ? BN : SEP_P ? 2 * BN : 0;    // + t * (SEP_P ? 64 : BN)
-  static constexpr uint32_t TMEM_P_STRIDE = SEP_P ? BN / 2 : BN;
-  static constexpr uint32_t TMEM_O = SINGLE ? BN + BN / 2 : SEP_P ? 3 * BN : 2 * BN;  // + t * D
+  // SINGLE: S [0,128), P [128,192), O [192,256). Otherwise S_t [t*128, t*128+128) with
+  // P_t over its first 64 columns, O_t [256 + t*128, 384 + t*128).
+  static constexpr uint32_t TMEM_P = SINGLE ? BN : 0;  // + t * BN when P overwrites S_t
+  static constexpr uint32_t TMEM_P_STRIDE = BN;
+  static constexpr uint32_t TMEM_O = SINGLE ? BN + BN / 2 : 2 * BN;  // + t * D
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);  // Q, K both K-major
   static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);   // V is MN-major
   static_assert(TMEM_O + Q_TILES * D <= TMEM_COLS, "TMEM budget");
@@ -134,18 +134,23 @@ struct Params {
   int window;  // local-window radius, or -1 for none
   int BH, num_qblocks;
   float scale_log2;  // scale * log2(e)
+  // fault-injection instantiation only (INJECT): the wait limit, and the K/V tile
+  // whose V copy the producer never issues
+  uint64_t inject_wait_ns;
+  int inject_skip_v_tile;
 };
 
 // Bounded wait on an mbarrier phase. Returns false (after recording `who`) if the
-// phase did not complete within kWaitLimitNs, or if another role already aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t who) {
+// phase did not complete within limit_ns, or if another role already aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t who,
+                                         uint64_t limit_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(&g_fault_word, who);
         return false;
@@ -198,7 +203,12 @@ __device__ __forceinline__ uint16_t* out_row_of(const Params& p, int b, int bh, 
 // HEADS_INTERLEAVED: Q, K, V and out are [B, n, h*d] (the projections' own layout,
 // before split_heads / after the concatenation of the heads) instead of [B, h, n, d];
 // the tensor maps then span (h*d, n, B) and a head is an x offset of h*d.
-template <int D, bool LOCAL, bool HEADS_INTERLEAVED, bool SINGLE>
+// INJECT: a test instantiation of the plain d = 64 kernel that exercises the
+// bounded-wait abort path: every wait gives up after p.inject_wait_ns, and the
+// producer stops before the V copy of K/V tile p.inject_skip_v_tile (after draining
+// the copies it did issue), so the PV issuer's wait for it runs out. The other
+// instantiations compile with the constant limit and no skip.
+template <int D, bool LOCAL, bool HEADS_INTERLEAVED, bool SINGLE, bool INJECT = false>
 __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_PER_SM)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -217,6 +227,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint64_t wlim = INJECT ? p.inject_wait_ns : kWaitLimitNs;
 
   // ---- which C::ROWS query rows of which (b, h): heaviest causal blocks first
   const int bh = blockIdx.x % p.BH;
@@ -254,9 +265,9 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
     ptx::mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(bar(C::B_KFULL + s), 1);
-      ptx::mbar_init(bar(C::B_KEMPTY + s), C::SEP_P ? 2 : 1);  // one arrival per MMA issuer
+      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);  // one arrival: the issuer that read the stage
       ptx::mbar_init(bar(C::B_VFULL + s), 1);
-      ptx::mbar_init(bar(C::B_VEMPTY + s), C::SEP_P ? 2 : 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(C::B_SFULL + t), 1);
@@ -300,13 +311,20 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       for (int j = 0; j < n_max && ok; ++j) {
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
-        ok = wait_bar(bar(C::B_KEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER);
+        ok = wait_bar(bar(C::B_KEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER, wlim);
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c)
           ptx::tma_load_3d(s_k + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + s),
                            tma_x + c * 64, (J0 + j) * BN, tma_z, pol_kv);
-        ok = wait_bar(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER);
+        if constexpr (INJECT) {
+          if (j == p.inject_skip_v_tile) {  // stop here: V_j is never copied
+            ok = false;
+            issued = 2 * j + 1;
+            break;
+          }
+        }
+        ok = wait_bar(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER, wlim);
         if (!ok) {
           issued = 2 * j + 1;
           break;
@@ -330,40 +348,26 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
     __syncwarp();
     } else if (warp >= C::WARP_MMA0 && warp < C::WARP_MMA0 + 4) {
     // ================================================================ MMA issuers
-    // SEP_P: warp 9 + t issues S_t, warp 11 + t issues PV_t. Otherwise warp 9 issues all.
+    // SINGLE: warp 5 (role 0) issues S, warp 7 (role 2) issues PV, each releasing the
+    // K or V stage it read. Otherwise warp 9 (role 0) issues everything.
     const int role = warp - C::WARP_MMA0;
-    const int t = role & 1;  // Q tile
-    const int n_t = t ? n_t1 : n_t0;
-    const int n_o = t ? n_t0 : n_t1;  // tiles of the other Q tile
-    const int off_t = t ? off1 : 0, off_o = t ? 0 : off1;  // ring use of each tile's first K/V tile
-    // a K/V stage (ring use u) the other Q tile never reads is released twice by this issuer
-    auto release = [&](int b0, int u) {
-      ptx::mma_commit(bar(b0 + u % C::STAGES));
-      if constexpr (LOCAL) {
-        if (u < off_o || u >= off_o + n_o) ptx::mma_commit(bar(b0 + u % C::STAGES));
-      } else {
-        if (u >= n_o) ptx::mma_commit(bar(b0 + u % C::STAGES));
-      }
-    };
-    if (C::SEP_P && role < 2 && lane == 0 && n_t > 0) {
-      // S_t(j) = Q_t K_j^T, as soon as K_j has landed and the softmax has loaded S_t(j-1)
-      const uint32_t q_tile = s_q + t * C::TILE_BYTES;
-      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
-      for (int j = 0; j < n_t && ok; ++j) {
-        const int u = off_t + j;
-        ok = wait_bar(bar(C::B_KFULL + u % C::STAGES), (u / C::STAGES) & 1, abort_flag, FAULT_MMA) &&
-             (j == 0 || wait_bar(bar(C::B_SFREE + t), (j - 1) & 1, abort_flag, FAULT_MMA));
+    if (SINGLE && role == 0 && lane == 0 && n_t0 > 0) {
+      // S(j) = Q K_j^T, as soon as K_j has landed and the softmax has loaded S(j-1)
+      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA, wlim);
+      for (int j = 0; j < n_t0 && ok; ++j) {
+        ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim) &&
+             (j == 0 || wait_bar(bar(C::B_SFREE), (j - 1) & 1, abort_flag, FAULT_MMA, wlim));
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t k_stage = s_k + (u % C::STAGES) * C::TILE_BYTES;
+        const uint32_t k_stage = s_k + (j % C::STAGES) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          ptx::mma_ss(tmem + t * BN, ptx::sdesc_sw128(q_tile + koff, 16, 1024),
-                      ptx::sdesc_sw128(k_stage + koff, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem, ptx::sdesc_sw128(s_q + koff, 16, 1024), ptx::sdesc_sw128(k_stage + koff, 16, 1024),
+                      C::IDESC_S, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(bar(C::B_SFULL + t));
-        release(C::B_KEMPTY, u);
+        ptx::mma_commit(bar(C::B_SFULL));
+        ptx::mma_commit(bar(C::B_KEMPTY + j % C::STAGES));
       }
       if (!ok) {
         // let every MMA already issued finish before TMEM is released
@@ -371,52 +375,51 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
         drain_wait(bar(C::B_DRAIN + role), 0);
       }
     }
-    if (C::SEP_P && role >= 2 && lane == 0 && n_t > 0) {
-      // O_t += P_t V_j once the softmax has stored P_t(j); P_t is the A operand, read from TMEM
-      const uint32_t a_p = tmem + C::TMEM_P + t * C::TMEM_P_STRIDE;
-      const uint32_t d_o = tmem + C::TMEM_O + t * D;
+    if (SINGLE && role == 2 && lane == 0 && n_t0 > 0) {
+      // O += P V_j once the softmax has stored P(j); P is the A operand, read from TMEM
+      const uint32_t a_p = tmem + C::TMEM_P;
+      const uint32_t d_o = tmem + C::TMEM_O;
       bool ok = true;
-      for (int j = 0; j < n_t && ok; ++j) {
-        const int u = off_t + j;
-        ok = wait_bar(bar(C::B_PFULL + t), j & 1, abort_flag, FAULT_MMA) &&
-             wait_bar(bar(C::B_VFULL + u % C::STAGES), (u / C::STAGES) & 1, abort_flag, FAULT_MMA);
+      for (int j = 0; j < n_t0 && ok; ++j) {
+        ok = wait_bar(bar(C::B_PFULL), j & 1, abort_flag, FAULT_MMA, wlim) &&
+             wait_bar(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t v_stage = s_v + (u % C::STAGES) * C::TILE_BYTES;
+        const uint32_t v_stage = s_v + (j % C::STAGES) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys = 16 rows of V = two 8-row swizzle groups
           ptx::mma_ts(d_o, a_p + kk * 8, ptx::sdesc_sw128(v_stage + kk * 2048, C::CHUNK_BYTES, 1024), C::IDESC_PV,
                       (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(bar(C::B_ODONE + t));
-        release(C::B_VEMPTY, u);
+        ptx::mma_commit(bar(C::B_ODONE));
+        ptx::mma_commit(bar(C::B_VEMPTY + j % C::STAGES));
       }
       if (!ok) {
         ptx::mma_commit(bar(C::B_DRAIN + role));
         drain_wait(bar(C::B_DRAIN + role), 0);
       }
     }
-    if (!C::SEP_P && !LOCAL && role == 0 && lane == 0 && n_max > 0) {
+    if (!SINGLE && !LOCAL && role == 0 && lane == 0 && n_max > 0) {
       // P_t lives in S_t, so S_t(j) must follow PV_t(j-1). One issuer runs, in order,
       //   PV0(j-1), S0(j), PV1(j-1), S1(j)
       // keeping each tile's hand-off short while the other tile's softmax runs.
       // (This issuer is on the critical path: keep its loop lean; the 2-way tile loop
       // must stay a plain counted loop so that it unrolls.)
       const int n_tt[2] = {n_t0, n_t1};
-      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
+      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA, wlim);
       ptx::tc_fence_after();
       for (int j = 0; j <= n_max && ok; ++j) {
         if (j < n_max) {
-          ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim);
           if (!ok) break;
         }
         if (j >= 1) {
-          ok = wait_bar(bar(C::B_VFULL + (j - 1) % C::STAGES), ((j - 1) / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          ok = wait_bar(bar(C::B_VFULL + (j - 1) % C::STAGES), ((j - 1) / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim);
           if (!ok) break;
         }
         ptx::tc_fence_after();
         for (int tt = 0; tt < 2; ++tt) {
           if (j >= 1 && j <= n_tt[tt]) {
-            ok = wait_bar(bar(C::B_PFULL + tt), (j - 1) & 1, abort_flag, FAULT_MMA);
+            ok = wait_bar(bar(C::B_PFULL + tt), (j - 1) & 1, abort_flag, FAULT_MMA, wlim);
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t v_stage = s_v + ((j - 1) % C::STAGES) * C::TILE_BYTES;
@@ -451,27 +454,27 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
         drain_wait(bar(C::B_DRAIN), 0);
       }
     }
-    if (!C::SEP_P && LOCAL && role == 0 && lane == 0 && n_max > 0) {
+    if (!SINGLE && LOCAL && role == 0 && lane == 0 && n_max > 0) {
       // the same issuer for the local-window instantiation, whose two Q tiles start at
       // different K/V tiles
       // Q tile tt uses ring uses [lo_tt[tt], hi_tt[tt]); j below is the ring use
       const int lo_tt[2] = {0, off1};
       const int hi_tt[2] = {n_t0, off1 + n_t1};
-      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA);
+      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA, wlim);
       ptx::tc_fence_after();
       for (int j = 0; j <= n_max && ok; ++j) {
         if (j < n_max) {
-          ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim);
           if (!ok) break;
         }
         if (j >= 1) {
-          ok = wait_bar(bar(C::B_VFULL + (j - 1) % C::STAGES), ((j - 1) / C::STAGES) & 1, abort_flag, FAULT_MMA);
+          ok = wait_bar(bar(C::B_VFULL + (j - 1) % C::STAGES), ((j - 1) / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim);
           if (!ok) break;
         }
         ptx::tc_fence_after();
         for (int tt = 0; tt < 2; ++tt) {
           if (j > lo_tt[tt] && j <= hi_tt[tt]) {
-            ok = wait_bar(bar(C::B_PFULL + tt), (j - 1 - lo_tt[tt]) & 1, abort_flag, FAULT_MMA);
+            ok = wait_bar(bar(C::B_PFULL + tt), (j - 1 - lo_tt[tt]) & 1, abort_flag, FAULT_MMA, wlim);
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t v_stage = s_v + ((j - 1) % C::STAGES) * C::TILE_BYTES;
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
     bool ok = true;
 
     for (int j = 0; j < n_tiles; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_SFULL + t), j & 1, abort_flag, FAULT_SOFTMAX));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_SFULL + t), j & 1, abort_flag, FAULT_SOFTMAX, wlim));
       if (!ok) break;
       ptx::tc_fence_after();
       uint32_t sr[4][32];
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       }
       const float mx = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
       const float m_tile = mx * c;
-      if (C::SEP_P) {  // S_t may now be overwritten by S_t(j+1)
+      if constexpr (SINGLE) {  // S may now be overwritten by S(j+1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(C::B_SFREE + t));
       }
@@ -582,7 +585,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       bool pv_done = (j == 0);  // PV_t(j-1) known to have completed
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O_t must hold PV_t(j-1) before it is rescaled in place
-        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX));
+        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
         if (!ok) break;
         pv_done = true;
         ptx::tc_fence_after();
@@ -617,9 +620,9 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       float l0, l1;
       ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
       l += l0 + l1;
-      if (C::SEP_P && !pv_done) {
-        // P_t is still the A operand of PV_t(j-1) until that MMA completes
-        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX));
+      if (SINGLE && !pv_done) {
+        // P is still the A operand of PV(j-1) until that MMA completes
+        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
         if (!ok) break;
         ptx::tc_fence_after();
       }
@@ -633,7 +636,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
     // ---------------------------------------------------------------- epilogue
     const bool row_valid = (row0 + t * BM < p.n_q) && (i < p.n_q);
     if (ok && n_tiles > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (n_tiles - 1) & 1, abort_flag, FAULT_EPILOGUE));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (n_tiles - 1) & 1, abort_flag, FAULT_EPILOGUE, wlim));
       if (ok) {
         ptx::tc_fence_after();
         const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
@@ -697,7 +700,13 @@ CUresult encode_map_interleaved(PFN_encodeTiled enc, CUtensorMap* map, const voi
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D, bool LOCAL, bool HEADS_INTERLEAVED, bool SINGLE = false>
+// One-shot arming of the INJECT instantiation for the next plain d = 64 attn_fwd call
+// on the arming host thread (attn_internal_arm_wait_timeout below).
+thread_local bool t_inject_armed = false;
+thread_local uint64_t t_inject_wait_ns = 0;
+thread_local int t_inject_skip_v_tile = 0;
+
+template <int D, bool LOCAL, bool HEADS_INTERLEAVED, bool SINGLE = false, bool INJECT = false>
 int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv) {
   using C = Cfg<D, SINGLE>;
   // the shared-memory opt-in is per device; set it once for each device used
@@ -705,7 +714,7 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE>,
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE, INJECT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
@@ -723,10 +732,12 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
   p.BH = a.B * a.H;
   p.num_qblocks = (a.n_q + C::ROWS - 1) / C::ROWS;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
+  p.inject_wait_ns = INJECT ? t_inject_wait_ns : kWaitLimitNs;
+  p.inject_skip_v_tile = INJECT ? t_inject_skip_v_tile : -1;
   const long long grid = (long long)p.BH * p.num_qblocks;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE, INJECT>
+      <<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -759,8 +770,15 @@ int launch(const TcArgs& a, PFN_encodeTiled enc) {
   // other CTA's softmax, which measured faster on short and long workloads alike (long
   // causal n = 8192: 282.8 -> 266.1 us against two Q tiles per CTA). The two-tile
   // kernel serves d = 128, where two CTAs do not fit one SM's shared memory.
-  if constexpr (D == 64) return launch_variant<D, false, false, true>(a, mq, mk, mv);
-  else return launch_variant<D, false, false>(a, mq, mk, mv);
+  if constexpr (D == 64) {
+    if (t_inject_armed) {
+      t_inject_armed = false;
+      return launch_variant<D, false, false, true, true>(a, mq, mk, mv);
+    }
+    return launch_variant<D, false, false, true>(a, mq, mk, mv);
+  } else {
+    return launch_variant<D, false, false>(a, mq, mk, mv);
+  }
 }
 
 }  // namespace
@@ -769,6 +787,12 @@ int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc) {
   if (a.d == 64) return launch<64>(a, enc);
   if (a.d == 128) return launch<128>(a, enc);
   return ATTN_ERR_UNSUPPORTED;
+}
+
+void arm_wait_timeout_injection(uint64_t wait_ns, int skip_v_tile) {
+  t_inject_wait_ns = wait_ns;
+  t_inject_skip_v_tile = skip_v_tile;
+  t_inject_armed = true;
 }
 
 int read_fault_word(cudaStream_t stream, int clear, uint32_t* out) {

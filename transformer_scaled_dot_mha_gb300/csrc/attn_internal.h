@@ -97,9 +97,19 @@ struct MhaArgs {
   cudaStream_t stream;
 };
 
+// One projection Y[M, N] = X[M, K] W[K, N] (+ bias[N]), bf16, row-major, validated.
+struct LinearJob {
+  const void* x;
+  const void* w;
+  const void* bias;  // nullptr: no bias
+  void* y;
+  int M, N, K;
+};
+
 int launch_attn_tc(const TcArgs& a, PFN_encodeTiled enc);   // attn_fwd_tc.cu
 int launch_attn_f32(const F32Args& a);                       // attn_fwd_f32.cu
 int read_fault_word(cudaStream_t stream, int clear, uint32_t* out);  // attn_fwd_tc.cu
+void arm_wait_timeout_injection(uint64_t wait_ns, int skip_v_tile);  // attn_fwd_tc.cu (tests only)
 int decode_splits(int B, int H, int n_q, int n_max, int d);               // attn_decode.cu
 int decode_chunk_keys(int B, int H, int n_max, int d);                    // attn_decode.cu
 size_t decode_workspace_bytes(int B, int H, int n_q, int n_max, int d);  // attn_decode.cu
@@ -112,6 +122,8 @@ bool bwd_fused(int d, int flags);                                        // attn
 size_t bwd_host_workspace_bytes(int B, int H, int n_q, int n_k, int d, int mask_mode, int flags);  // attn_bwd_host.cu
 int launch_attn_bwd_host(const BwdArgs& a, PFN_encodeTiled enc, void* workspace);                 // attn_bwd_host.cu
 int read_bwd_fault_word(int clear, uint32_t* out);                       // attn_bwd.cu
+int launch_linear(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cudaStream_t stream);  // attn_linear.cu
+int read_linear_fault_word(int clear, uint32_t* out);                    // attn_linear.cu
 size_t mha_workspace_bytes(int B, int n_q, int n_k, int H, int d);         // attn_mha.cu
 int launch_attn_mha(const MhaArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_mha.cu
 // Host-operand pipelines (attn_host.cu, attn_bwd_host.cu): chunks of the flattened

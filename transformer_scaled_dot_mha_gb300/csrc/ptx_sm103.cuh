@@ -84,6 +84,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared, as tma_load_3d with two coordinates.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y,
+                                            uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(cache_hint)
+      : "memory");
+}
+
 // 3-D tiled reduce-add shared -> global (element type of the tensor map), tracked
 // by the bulk async-group of the issuing thread. Elements outside the tensor are
 // skipped. Coordinates as in tma_load_3d; they must not be negative.
@@ -93,6 +103,17 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// 2-D tiled tensor copy shared -> global, tracked by the bulk async-group of the
+// issuing thread. Elements outside the tensor are not written. Coordinates as in
+// tma_load_2d; they must not be negative.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+// The shared-memory sources of all but the newest bulk group of this thread have been read.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The shared-memory sources of this thread's bulk groups have been read.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
