@@ -79,6 +79,23 @@ def test_linear_matches_oracle(orc, M, N, K, bias):
     check(orc, x, w, b, run(x, w, b))
 
 
+def test_linear_cluster_path_odd_row_blocks(orc):
+    """A launch of at least 1024 tiles runs as 2-CTA clusters (row blocks 2u, 2u + 1
+    share each W tile). 33 row blocks (M = 4103) x 32 column blocks: the last pair's
+    second CTA lies wholly past M and must write nothing; sampled rows of every row
+    block edge against the oracle, and the rows past M of a guarded buffer untouched."""
+    M, N, K = 4103, 8192, 64
+    x, w, b = draw(9300, M, N, K)
+    pad_rows = 40
+    buf = torch.full(((M + pad_rows) * N,), -7.0, dtype=torch.bfloat16, device="cuda")
+    y = buf[:M * N].view(M, N)
+    attn.attn_linear(dev(x), dev(w), y, dev(b))
+    torch.cuda.synchronize()
+    assert torch.all(buf[M * N:] == -7.0)
+    rows = sorted({0, 1, 127, 128, M // 2, 4095, 4096, M - 2, M - 1} | set(range(5, M, 37)))
+    check(orc, x, w, b, y.float().cpu().numpy().astype(np.float64), np.array(rows))
+
+
 def test_linear_guard_bands_and_determinism():
     """Nothing is written outside y, and two calls give identical bits."""
     x, w, b = draw(9100, 300, 264, 136)

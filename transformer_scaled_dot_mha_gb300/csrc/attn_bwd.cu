@@ -61,6 +61,7 @@ constexpr int EW_THREADS = 256;
 constexpr int WARP_LOAD = 8, WARP_MMA = 9;
 constexpr int WARP_DRAIN = 12;  // fused: warps 12-15 drain the dQ partials (warp 11 idles)
 constexpr int kMaxDevices = 64;
+constexpr int kHeadGroup = 4;  // heads whose CTAs run together (L2 holds their streams and dQ sums)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t FAULT_BWD = 32;
@@ -121,6 +122,7 @@ struct BwdParams {
   uint16_t* g1;        // dkdv: dV [BH][n_k][D]
   const int32_t* key_lens;
   int H, n_q, n_k, mask_mode, BH, tiles, q_tiles;
+  int group;  // heads per group of the CTA order (see the kernel)
   float scale, scale_log2;
 };
 
@@ -245,10 +247,16 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
   float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [S][-lse log2(e)[T], -D[T]]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bh = blockIdx.x % p.BH;
-  // own tile: keys (DKDV; the low, busiest causal tiles first) or queries (dQ; the
-  // high, busiest causal tiles first)
-  const int own = DKDV ? (int)(blockIdx.x / p.BH) : p.tiles - 1 - (int)(blockIdx.x / p.BH);
+  // CTA order: groups of p.group heads, one after the other; within a group the own
+  // tiles busiest first -- keys (DKDV: the low causal tiles) or queries (dQ: the high
+  // ones) -- with the group's heads interleaved. The CTAs resident at one time then
+  // work on a few heads, whose streamed tiles and fp32 dQ accumulators stay in L2.
+  const int per_group = p.group * p.tiles;
+  const int grp = (int)(blockIdx.x / per_group);
+  const int gsize = min(p.group, p.BH - grp * p.group);
+  const int within = (int)(blockIdx.x - (unsigned)grp * per_group);
+  const int bh = grp * p.group + within % gsize;
+  const int own = DKDV ? within / gsize : p.tiles - 1 - within / gsize;
   const int b = bh / p.H;
   const bool causal = (p.mask_mode & 1) != 0;
   int kv_len = p.n_k;
@@ -753,6 +761,7 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_ac
   p.n_k = a.n_k;
   p.mask_mode = a.mask_mode;
   p.BH = BH;
+  p.group = BH < kHeadGroup ? (int)BH : kHeadGroup;
   p.scale = a.scale;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   // dK, dV: own = key tiles; A0 = K, A1 = V; streamed R0 = Q, R1 = dO

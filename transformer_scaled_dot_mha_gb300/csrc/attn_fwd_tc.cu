@@ -560,6 +560,95 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
           for (int x = 0; x < 32; ++x)
             if (q4 * 32 + x >= lim || q4 * 32 + x < first) sr[q4][x] = __float_as_uint(-INFINITY);
       }
+      bool pv_done;
+      uint32_t pk[2][32];
+      if constexpr (SINGLE) {
+        // d = 64: after the first tile the exponentials are taken against the current
+        // reference maximum while the tile's maximum is formed beside them (the two are
+        // independent); only a row whose maximum grows past the threshold (rare after
+        // the first tile) redoes them against the new reference. Same results bit for
+        // bit; the maximum leaves the per-tile dependency chain. At d = 128 this measured
+        // slower (the softmax warps' registers run out), so that path keeps the order
+        // maximum -> exponentials.
+      // row maximum: eight independent 3-input max chains over 16 columns each
+      auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
+      auto row_max = [&]() -> float {
+        float mc[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+          mc[a] = fmaxf(col(a, 0), col(a, 1));
+#pragma unroll
+          for (int x = 2; x < 16; x += 2) mc[a] = ptx::max3(mc[a], col(a, x), col(a, x + 1));
+        }
+        return ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * c;
+      };
+      auto exps = [&](float m_now) -> float {
+        const float m_use = (m_now == -INFINITY) ? 0.0f : m_now;
+        const uint64_t c2 = ptx::f2_pack(c, c);
+        const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+        uint64_t part[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const uint64_t sx = ptx::f2_pack(__uint_as_float(sr[q4][x]), __uint_as_float(sr[q4][x + 1]));
+            float a0, a1;
+            ptx::f2_unpack(ptx::f2_fma(sx, c2, negm2), a0, a1);
+            const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+            part[q4] = ptx::f2_add(part[q4], ptx::f2_pack(p0, p1));
+            pk[q4 >> 1][(q4 & 1) * 16 + (x >> 1)] = ptx::pack_bf16x2(p0, p1);
+          }
+        float l0, l1;
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
+        return l0 + l1;
+      };
+      auto s_free = [&](float dep) {
+        if constexpr (SINGLE) {  // S may now be overwritten by S(j+1)
+          ptx::tc_fence_before();
+          ptx::mbar_arrive_after(bar(C::B_SFREE + t), dep);
+        }
+      };
+      pv_done = (j == 0);  // PV_t(j-1) known to have completed
+      float l_tile;
+      if (j == 0) {
+        const float m_tile = row_max();
+        s_free(m_tile);
+        if (m_tile > m_ref + kRescaleThreshold) {  // l is still 0
+          m_ref = m_tile;
+        }
+        l_tile = exps(m_ref);
+      } else {
+        // against the current reference: the result stands unless a row maximum grows
+        l_tile = exps(m_ref);
+        const float m_tile = row_max();
+        s_free(m_tile);
+        const bool grow = m_tile > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {
+          float alpha = 1.0f;
+          if (grow) {
+            alpha = ptx::ex2(m_ref - m_tile);  // 0 when m_ref is still -inf
+            l *= alpha;
+            m_ref = m_tile;
+          }
+          // O_t must hold PV_t(j-1) before it is rescaled in place
+          ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
+          if (!ok) break;
+          pv_done = true;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t o[32];
+            ptx::tmem_ld32(t_o + q4 * 32, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+            ptx::tmem_st32(t_o + q4 * 32, o);
+          }
+          l_tile = exps(m_ref);
+        }
+      }
+      l += l_tile;
+      } else {
       // row maximum: eight independent 3-input max chains over 16 columns each
       auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
       float mc[8];
@@ -582,7 +671,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
         l *= alpha;
         m_ref = m_tile;
       }
-      bool pv_done = (j == 0);  // PV_t(j-1) known to have completed
+      pv_done = (j == 0);  // PV_t(j-1) known to have completed
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O_t must hold PV_t(j-1) before it is rescaled in place
         ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
@@ -605,7 +694,6 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       const uint64_t c2 = ptx::f2_pack(c, c);
       const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
       uint64_t part[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[2][32];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
@@ -620,6 +708,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       float l0, l1;
       ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
       l += l0 + l1;
+      }
       if (SINGLE && !pv_done) {
         // P is still the A operand of PV(j-1) until that MMA completes
         ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));

@@ -24,8 +24,10 @@
 //               M128 N256 K16 tcgen05.mma per K step into one of two 256-column
 //               fp32 accumulators, and releases each ring stage with a commit;
 //   warps 2-5   epilogue (thread = output row = TMEM lane): load the accumulator
-//               32 columns at a time, add the bias in fp32, round to bf16 (nearest
-//               even) and store 16-byte pieces of the row; then hand the
+//               64 columns at a time, add the bias in fp32, round to bf16 (nearest
+//               even), write the warp's 32 x 64 slab into one of its two 128-byte-
+//               swizzled staging buffers and store it with one TMA tensor store
+//               (coalesced, tails clipped by the tensor map); then hand the
 //               accumulator back, so that it drains while the MMAs fill the other.
 // Every mbarrier wait is bounded in time; a wait that runs out records a fault bit
 // (attn_fault_status), raises the CTA's abort flag, and every role stops: the
@@ -55,7 +57,9 @@ constexpr int B_BOX_BYTES = BK * 64 * 2;           // 8 KB: 64 K rows x 64 colum
 constexpr int B_BYTES = (BN / 64) * B_BOX_BYTES;   // 32 KB
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+constexpr int STG_BYTES = 32 * 64 * 2;             // one 32-row x 64-column bf16 slab
+constexpr int OFF_STG = OFF_B + STAGES * B_BYTES;  // two slabs per epilogue warp
+constexpr int OFF_BAR = OFF_STG + 4 * 2 * STG_BYTES;
 constexpr int B_FULL = 0, B_EMPTY = STAGES, B_ACC_FULL = 2 * STAGES, B_ACC_EMPTY = 2 * STAGES + 2,
               B_DRAIN = 2 * STAGES + 4;
 constexpr int NUM_BARS = 2 * STAGES + 5;
@@ -69,6 +73,10 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr uint32_t FAULT_LINEAR = 128;
+// Launches of at least this many 128 x 256 tiles run as 2-CTA clusters sharing each W
+// tile (same-box A/B: +5-6 % on 16384 x 2048 x 2048 and on the three Q/K/V projections
+// at 16384 x 1024; -2 % on a single 16384 x 1024 x 1024 projection of 512 tiles).
+constexpr long long kClusterMinTiles = 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct LinProblem {
@@ -82,8 +90,8 @@ struct LinProblem {
 struct LinParams {
   LinProblem pr[3];
   int n_prob;
-  int total_tiles;
-  int interleave;  // all problems share M and N: list order (row block, problem, column block)
+  int total_tiles;  // units of CL row blocks x one column block
+  int interleave;  // all problems share M and N: list order (row unit, problem, column block)
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -108,7 +116,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) return;
 }
 
-// Tile t of the list -> problem z, row block mb, column block nb.
+// Tile t of the list -> problem z, row unit mu (CL row blocks), column block nb.
 __device__ __forceinline__ void tile_of(const LinParams& p, int t, int& z, int& mb, int& nb) {
   if (p.interleave) {
     const int nbk = p.pr[0].n_blocks;
@@ -125,11 +133,18 @@ __device__ __forceinline__ void tile_of(const LinParams& p, int t, int& z, int& 
   }
 }
 
+// CL: CTAs per cluster. With CL = 2 the two CTAs of a cluster take row blocks 2u and
+// 2u + 1 of the same column block: each loads its own X rows and half of the W tile,
+// multicast into both CTAs, so each CTA's L2 traffic per K step drops from 48 to 32 KB.
+// A ring stage is then free only once both CTAs' MMAs have read it (the issuers commit
+// to the stage's barrier in both CTAs), and cluster barriers bracket the CTAs' lives.
+template <int CL>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_linear_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_w0,
-                       const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_w1,
+                       const __grid_constant__ CUtensorMap tm_y0, const __grid_constant__ CUtensorMap tm_x1,
+                       const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_y1,
                        const __grid_constant__ CUtensorMap tm_x2, const __grid_constant__ CUtensorMap tm_w2,
-                       const __grid_constant__ LinParams p) {
+                       const __grid_constant__ CUtensorMap tm_y2, const __grid_constant__ LinParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((ptx::smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(&g_linear_fault_word, FAULT_LINEAR);
@@ -145,7 +160,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(bar(B_FULL + s), 1);
-      ptx::mbar_init(bar(B_EMPTY + s), 1);
+      ptx::mbar_init(bar(B_EMPTY + s), CL);  // one commit from the MMA issuer of each CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bar(B_ACC_FULL + b), 1);
@@ -162,19 +177,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tm_x0);
     ptx::prefetch_tmap(&tm_w0);
+    ptx::prefetch_tmap(&tm_y0);
     if (p.n_prob > 1) {
       ptx::prefetch_tmap(&tm_x1);
       ptx::prefetch_tmap(&tm_w1);
+      ptx::prefetch_tmap(&tm_y1);
     }
     if (p.n_prob > 2) {
       ptx::prefetch_tmap(&tm_x2);
       ptx::prefetch_tmap(&tm_w2);
+      ptx::prefetch_tmap(&tm_y2);
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (CL > 1) ptx::cluster_sync();  // the peer's barriers exist before any multicast
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int rank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
+  const int unit0 = (int)(blockIdx.x / CL), units_step = (int)(gridDim.x / CL);
+  constexpr uint16_t kPeers = (uint16_t)((1u << CL) - 1);
 
   if (warp == 0) {
     // ================================================================ producer
@@ -182,9 +204,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol = ptx::policy_evict_last();  // X rows and W are each read by several CTAs
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        int z, mb, nb;
-        tile_of(p, t, z, mb, nb);
+      for (int t = unit0; t < p.total_tiles && ok; t += units_step) {
+        int z, mu, nb;
+        tile_of(p, t, z, mu, nb);
+        const int mb = mu * CL + rank;
         const CUtensorMap* tx = z == 0 ? &tm_x0 : z == 1 ? &tm_x1 : &tm_x2;
         const CUtensorMap* tw = z == 0 ? &tm_w0 : z == 1 ? &tm_w1 : &tm_w2;
         const int k_steps = (p.pr[z].K + BK - 1) / BK;
@@ -196,10 +219,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           ptx::mbar_arrive_expect_tx(bar(B_FULL + s), A_BYTES + B_BYTES);
           ptx::tma_load_2d(s_a + s * A_BYTES, tx, bar(B_FULL + s), kb * BK, mb * BM, pol);
+          if constexpr (CL == 1) {
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            ptx::tma_load_2d(s_b + s * B_BYTES + c * B_BOX_BYTES, tw, bar(B_FULL + s), nb * BN + c * 64, kb * BK,
-                             pol);
+            for (int c = 0; c < BN / 64; ++c)
+              ptx::tma_load_2d(s_b + s * B_BYTES + c * B_BOX_BYTES, tw, bar(B_FULL + s), nb * BN + c * 64, kb * BK,
+                               pol);
+          } else {  // this CTA's share of the W boxes, into every CTA of the cluster
+#pragma unroll
+            for (int c = rank * (BN / 64 / CL); c < (rank + 1) * (BN / 64 / CL); ++c)
+              ptx::tma_load_2d_mc(s_b + s * B_BYTES + c * B_BOX_BYTES, tw, bar(B_FULL + s), nb * BN + c * 64,
+                                  kb * BK, kPeers, pol);
+          }
         }
       }
       if (!ok) {
@@ -215,9 +245,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t it = 0;
       int lt = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++lt) {
-        int z, mb, nb;
-        tile_of(p, t, z, mb, nb);
+      for (int t = unit0; t < p.total_tiles && ok; t += units_step, ++lt) {
+        int z, mu, nb;
+        tile_of(p, t, z, mu, nb);
         const int buf = lt & 1;
         ok = wait_bar(bar(B_ACC_EMPTY + buf), ((lt >> 1) & 1) ^ 1, abort_flag);
         if (!ok) break;
@@ -234,7 +264,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < BK / 16; ++kk)  // 16 K = 32 bytes of an X row = 16 rows of W
             ptx::mma_ss(d, ptx::sdesc_sw128(a_st + kk * 32, 16, 1024),
                         ptx::sdesc_sw128(b_st + kk * 2048, B_BOX_BYTES, 1024), IDESC, (kb | kk) ? 1u : 0u);
-          ptx::mma_commit(bar(B_EMPTY + s));
+          if constexpr (CL == 1)
+            ptx::mma_commit(bar(B_EMPTY + s));
+          else
+            ptx::mma_commit_mc(bar(B_EMPTY + s), kPeers);
         }
         if (!ok) break;
         ptx::mma_commit(bar(B_ACC_FULL + buf));
@@ -249,64 +282,69 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ================================================================ epilogue
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may read
-    const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t stg = s_base + OFF_STG + (warp - 2) * 2 * STG_BYTES;
+    int sb = 0;  // staging slab to fill next
     int lt = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++lt) {
-      int z, mb, nb;
-      tile_of(p, t, z, mb, nb);
+    for (int t = unit0; t < p.total_tiles; t += units_step, ++lt) {
+      int z, mu, nb;
+      tile_of(p, t, z, mu, nb);
+      const int mb = mu * CL + rank;
       const int buf = lt & 1;
       if (!__all_sync(0xffffffffu, wait_bar(bar(B_ACC_FULL + buf), (lt >> 1) & 1, abort_flag))) break;
       ptx::tc_fence_after();
       const LinProblem& P = p.pr[z];
-      const int row = mb * BM + r;
-      const bool row_ok = row < P.M;
-      uint16_t* yrow = P.y + (size_t)(row_ok ? row : 0) * P.N;
+      const CUtensorMap* ty = z == 0 ? &tm_y0 : z == 1 ? &tm_y1 : &tm_y2;
+      // rows of this warp's slabs inside Y (the second CTA of a pair can lie wholly past M)
+      const bool row_ok = mb * BM + quarter * 32 < P.M;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld32(tmem + lane_off + buf * BN + c * 32, v);
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t v[64];
+        ptx::tmem_ld32(tmem + lane_off + buf * BN + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        ptx::tmem_ld32(tmem + lane_off + buf * BN + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         ptx::tmem_wait_ld();
-        const int col0 = nb * BN + c * 32;
-        if (col0 < P.N) {
-          float bias[32];
-          if (P.bias) {
+        const int col0 = nb * BN + c * 64;
+        if (col0 < P.N && row_ok) {
+          uint32_t w[32];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              uint4 bw = make_uint4(0, 0, 0, 0);
-              if (col0 + 8 * x < P.N) bw = __ldg(reinterpret_cast<const uint4*>(P.bias + col0) + x);
-              const uint32_t w4[4] = {bw.x, bw.y, bw.z, bw.w};
+          for (int x = 0; x < 8; ++x) {  // eight columns (one 16-byte bias piece) at a time
+            uint4 bw = make_uint4(0, 0, 0, 0);
+            if (P.bias && col0 + 8 * x < P.N) bw = __ldg(reinterpret_cast<const uint4*>(P.bias + col0) + x);
+            const uint32_t b4[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                bias[8 * x + 2 * e] = __uint_as_float(w4[e] << 16);
-                bias[8 * x + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) bias[x] = 0.0f;
+            for (int e = 0; e < 4; ++e)
+              w[4 * x + e] = ptx::pack_bf16x2(__uint_as_float(v[8 * x + 2 * e]) + __uint_as_float(b4[e] << 16),
+                                              __uint_as_float(v[8 * x + 2 * e + 1]) +
+                                                  __uint_as_float(b4[e] & 0xffff0000u));
           }
-          uint32_t w[16];
+          // the slab is free once the store issued from it two rounds ago has read it
+          if (lane == 0) ptx::bulk_wait_read1();
+          __syncwarp();
+          const uint32_t slab = stg + sb * STG_BYTES;
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
-            w[x] = ptx::pack_bf16x2(__uint_as_float(v[2 * x]) + bias[2 * x],
-                                    __uint_as_float(v[2 * x + 1]) + bias[2 * x + 1]);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + col0);
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-              if (col0 + 8 * x < P.N) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          for (int x = 0; x < 8; ++x)  // 128-byte swizzle: 16-byte piece x of row r goes to x ^ (r & 7)
+            ptx::st_shared_v4(slab + lane * 128 + ((x ^ (lane & 7)) << 4), w[4 * x], w[4 * x + 1], w[4 * x + 2],
+                              w[4 * x + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(ty, slab, col0, mb * BM + quarter * 32);
+            ptx::bulk_commit();
           }
+          sb ^= 1;
         }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(B_ACC_EMPTY + buf));
     }
+    if (lane == 0) ptx::bulk_wait0();  // every store has landed before the CTA exits
+    __syncwarp();
   }
 
   // ---- teardown
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (CL > 1) ptx::cluster_sync();  // no CTA leaves while its peer may still write to it
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
@@ -324,6 +362,17 @@ CUresult encode_x(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int M
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Y [M, N] row-major, stored by the epilogue: the map spans (N, M), box 64 x 32.
+CUresult encode_y(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int M, int N) {
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 // W [K, N] row-major: the map spans (N, K), box 64 x 64.
 CUresult encode_w(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int K, int N) {
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
@@ -335,38 +384,53 @@ CUresult encode_w(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int K
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-int sm_count(int dev) {
+// Persistent grid of CL-CTA clusters: as many as can be resident at once.
+template <int CL>
+int resident_clusters(int dev) {
   static std::atomic<int> cached[kMaxDevices];
   int n = cached[dev].load(std::memory_order_relaxed);
   if (n > 0) return n;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  if (CL == 1) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL * 64);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = CL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_linear_kernel<CL>, &cfg) != cudaSuccess) return 0;
+  }
+  if (n <= 0) return 0;
   cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
-}  // namespace
-
-int launch_linear(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cudaStream_t stream) {
-  if (n_jobs < 1 || n_jobs > 3) return ATTN_ERR_INVALID;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+template <int CL>
+int launch_linear_cl(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cudaStream_t stream, int dev) {
   static std::atomic<bool> attr_done[kMaxDevices];
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attn_linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+    if (cudaFuncSetAttribute(attn_linear_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
         cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_done[dev].store(true, std::memory_order_release);
   }
-  const int sms = sm_count(dev);
-  if (sms <= 0) return ATTN_ERR_CUDA;
-  CUtensorMap mx[3], mw[3];
+  const int clusters = resident_clusters<CL>(dev);
+  if (clusters <= 0) return ATTN_ERR_CUDA;
+  CUtensorMap mx[3], mw[3], my[3];
   LinParams p{};
   p.n_prob = n_jobs;
   long long tiles = 0;
   bool same = true;
   for (int z = 0; z < n_jobs; ++z) {
     const LinearJob& j = jobs[z];
-    if (encode_x(enc, &mx[z], j.x, j.M, j.K) != CUDA_SUCCESS || encode_w(enc, &mw[z], j.w, j.K, j.N) != CUDA_SUCCESS)
+    if (encode_x(enc, &mx[z], j.x, j.M, j.K) != CUDA_SUCCESS || encode_w(enc, &mw[z], j.w, j.K, j.N) != CUDA_SUCCESS ||
+        encode_y(enc, &my[z], j.y, j.M, j.N) != CUDA_SUCCESS)
       return ATTN_ERR_UNSUPPORTED;
     LinProblem& P = p.pr[z];
     P.y = static_cast<uint16_t*>(j.y);
@@ -376,20 +440,49 @@ int launch_linear(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cudaSt
     P.K = j.K;
     P.n_blocks = (j.N + BN - 1) / BN;
     P.tile_begin = (int)tiles;
-    tiles += (long long)((j.M + BM - 1) / BM) * P.n_blocks;
+    const long long m_units = ((long long)(j.M + BM - 1) / BM + CL - 1) / CL;
+    tiles += m_units * P.n_blocks;
     if (tiles > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     same = same && j.M == jobs[0].M && j.N == jobs[0].N;
   }
   for (int z = n_jobs; z < 3; ++z) {  // unused slots repeat the first problem's maps
     mx[z] = mx[0];
     mw[z] = mw[0];
+    my[z] = my[0];
     p.pr[z] = p.pr[0];
   }
   p.total_tiles = (int)tiles;
   p.interleave = (n_jobs > 1 && same) ? 1 : 0;
-  const int grid = (int)(tiles < sms ? tiles : sms);
-  attn_linear_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mx[0], mw[0], mx[1], mw[1], mx[2], mw[2], p);
+  const int grid = CL * (int)(tiles < clusters ? tiles : clusters);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_linear_kernel<CL>, mx[0], mw[0], my[0], mx[1], mw[1], my[1], mx[2], mw[2], my[2],
+                         p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_linear(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cudaStream_t stream) {
+  if (n_jobs < 1 || n_jobs > 3) return ATTN_ERR_INVALID;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  long long tiles = 0;
+  for (int z = 0; z < n_jobs; ++z)
+    tiles += (long long)((jobs[z].M + BM - 1) / BM) * ((jobs[z].N + BN - 1) / BN);
+  if (tiles >= kClusterMinTiles) return launch_linear_cl<2>(jobs, n_jobs, enc, stream, dev);
+  return launch_linear_cl<1>(jobs, n_jobs, enc, stream, dev);
 }
 
 int read_linear_fault_word(int clear, uint32_t* out) {
