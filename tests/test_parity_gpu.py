@@ -260,3 +260,16 @@ def test_bf16_long_cross_key_length_edges(orc, d, lens):
     ids = _sample_rows(w.B, w.H, w.n_q)
     ref, ref_lse = orc.attention_rows(q, k, v, w.scale, ids, P, kl)
     assert_bf16_close(out.reshape(-1, w.d_v)[ids], lse.reshape(-1)[ids], ref, ref_lse)
+
+
+@pytest.mark.parametrize("mode,n_q,n_k", [(C | P, 777, 777), (P, 900, 1300), (C, 1025, 1025)])
+def test_bf16_multi_wave_grid(orc, mode, n_q, n_k):
+    """More than one wave of 128-row Q tiles (here 336-432 CTAs on 2 x 152 slots), with
+    key lengths of 0, 1 and a tile edge: CTAs with no K/V tile or a single key run
+    beside ordinary ones and in the second wave. Every row against the oracle."""
+    B, H = 3, 16
+    w, (q, k, v, _) = gen("cross_pad_b16_h16_q256_k512_d64", seed=5000 + n_q + mode, B=B, H=H, n_q=n_q, n_k=n_k)
+    kl = np.array([0, 1, min(n_k, 640)], np.int32) if mode & P else np.full(B, n_k, np.int32)
+    out, lse = run_bf16(q, k, v, kl, w.scale, mode)
+    ref, ref_lse = orc.attention(q, k, v, w.scale, mode, kl)
+    assert_bf16_close(out, lse, ref, ref_lse)
