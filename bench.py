@@ -83,11 +83,17 @@ KERNEL_SOURCES = {
     "attn_bwd_tc_kernel": ("attn_bwd.cu", "ptx_sm103.cuh"),
 }
 NCU_TRAFFIC = {
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "9d293e72bec9d960"): 146398976,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 152260608,
+    ("long_none_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 115189504,
+    ("long_causal_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 573938688,
+    ("long_none_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 1067328512,
+    ("long_cross_pad_b2_h16_q4096_k8192_d64", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 76296704,
+    ("long_cross_pad_b2_h16_q4096_k8192_d128", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 529853440,
+    ("local_causal_b2_h16_n8192_d64_w511", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 110792960,
     # the warp kernel only (the merge kernel is not counted)
-    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "a3b9d57c7afa8ca3"): 424485376,
+    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "b13c232734a09acc"): 424487936,
     # the fused d = 64 kernel
-    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "f4b90b7e38fe3b46"): 1059860224,
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "865f9a0a58f45e0d"): 291904512,
 }
 
 
@@ -95,10 +101,11 @@ _C_COMMENT = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
 
 
 def _code_only(src: str) -> str:
-    """C++ source without its comments and blank lines (string literals kept): DRAM
-    traffic depends on the code, so a comment edit must not invalidate a capture."""
+    """C++ source without its comments, blank lines and the whitespace at either end of a
+    line (string literals kept): DRAM traffic depends on the code, so a comment or
+    indentation edit must not invalidate a capture."""
     s = _C_COMMENT.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", src)
-    return "\n".join(line.rstrip() for line in s.splitlines() if line.strip())
+    return "\n".join(line.strip() for line in s.splitlines() if line.strip())
 
 
 def kernel_source_hash(kernel: str = "attn_fwd_tc_kernel") -> str:

@@ -65,12 +65,13 @@ def test_single_process_helpers():
 
 def test_kernel_source_hash_ignores_comments_only():
     """The DRAM traffic the bench reports is keyed by a hash of the kernel sources; a
-    comment or blank-line edit must keep the key, any code edit must change it."""
+    comment, blank-line or indentation edit must keep the key, any code edit must change it."""
     import bench
 
     code = 'int f(int x) {\n  // scale\n  return 2 * x; /* twice */\n}\nconst char* s = "// kept";\n'
     assert bench._code_only(code) == bench._code_only(code.replace("// scale", "// doubled\n\n"))
     assert "// kept" in bench._code_only(code)                     # a string literal is code
     assert bench._code_only(code) != bench._code_only(code.replace("2 * x", "3 * x"))
+    assert bench._code_only(code) == bench._code_only(code.replace("  return", "      return"))
     for k in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(k)) == 16

@@ -58,6 +58,7 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain copies in flight
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale when max grows > 2^8
+constexpr int kHeadGroup = 8;                      // heads per launch group (non-causal one-tile kernel)
 
 constexpr uint32_t FAULT_PRODUCER = 1, FAULT_MMA = 2, FAULT_SOFTMAX = 4, FAULT_EPILOGUE = 8;
 constexpr uint32_t FAULT_SMEM_ALIGN = 64;  // dynamic shared memory not 1024-byte aligned
@@ -133,6 +134,7 @@ struct Params {
   int H, n_q, n_k, mask_mode;
   int window;  // local-window radius, or -1 for none
   int BH, num_qblocks;
+  int head_group;    // heads whose CTAs are launched together (BH: one group)
   float scale_log2;  // scale * log2(e)
   // fault-injection instantiation only (INJECT): the wait limit, and the K/V tile
   // whose V copy the producer never issues
@@ -229,9 +231,20 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
   const int lane = threadIdx.x & 31;
   const uint64_t wlim = INJECT ? p.inject_wait_ns : kWaitLimitNs;
 
-  // ---- which C::ROWS query rows of which (b, h): heaviest causal blocks first
-  const int bh = blockIdx.x % p.BH;
-  const int qb = p.num_qblocks - 1 - blockIdx.x / p.BH;
+  // ---- which C::ROWS query rows of which (b, h): groups of p.head_group heads one after
+  // the other, within a group the heaviest causal blocks first with its heads interleaved
+  int bh, qb;
+  if constexpr (SINGLE && !LOCAL) {
+    const int per_group = p.head_group * p.num_qblocks;
+    const int grp = (int)(blockIdx.x / per_group);
+    const int gsize = min(p.head_group, p.BH - grp * p.head_group);
+    const int within = (int)(blockIdx.x - (unsigned)grp * per_group);
+    bh = grp * p.head_group + within % gsize;
+    qb = p.num_qblocks - 1 - within / gsize;
+  } else {
+    bh = blockIdx.x % p.BH;
+    qb = p.num_qblocks - 1 - blockIdx.x / p.BH;
+  }
   const int b = bh / p.H;
   const int tma_z = HEADS_INTERLEAVED ? b : bh;                   // TMA z coordinate of this head
   const int tma_x = HEADS_INTERLEAVED ? (bh - b * p.H) * D : 0;  // and its x offset
@@ -562,17 +575,95 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       }
       bool pv_done;
       uint32_t pk[2][32];
-      if constexpr (SINGLE) {
+      if constexpr (SINGLE && !LOCAL) {
         // d = 64: after the first tile the exponentials are taken against the current
         // reference maximum while the tile's maximum is formed beside them (the two are
         // independent); only a row whose maximum grows past the threshold (rare after
         // the first tile) redoes them against the new reference. Same results bit for
-        // bit; the maximum leaves the per-tile dependency chain. At d = 128 this measured
-        // slower (the softmax warps' registers run out), so that path keeps the order
-        // maximum -> exponentials.
-      // row maximum: eight independent 3-input max chains over 16 columns each
-      auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
-      auto row_max = [&]() -> float {
+        // bit; the maximum leaves the per-tile dependency chain. At d = 128 (the softmax
+        // warps' registers run out) and with a local window (-6 %) this measured slower,
+        // so those paths keep the order maximum -> exponentials.
+        // row maximum: eight independent 3-input max chains over 16 columns each
+        auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
+        auto row_max = [&]() -> float {
+          float mc[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) {
+            mc[a] = fmaxf(col(a, 0), col(a, 1));
+#pragma unroll
+            for (int x = 2; x < 16; x += 2) mc[a] = ptx::max3(mc[a], col(a, x), col(a, x + 1));
+          }
+          return ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * c;
+        };
+        auto exps = [&](float m_now) -> float {
+          const float m_use = (m_now == -INFINITY) ? 0.0f : m_now;
+          const uint64_t c2 = ptx::f2_pack(c, c);
+          const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+          uint64_t part[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+            for (int x = 0; x < 32; x += 2) {
+              const uint64_t sx = ptx::f2_pack(__uint_as_float(sr[q4][x]), __uint_as_float(sr[q4][x + 1]));
+              float a0, a1;
+              ptx::f2_unpack(ptx::f2_fma(sx, c2, negm2), a0, a1);
+              const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+              part[q4] = ptx::f2_add(part[q4], ptx::f2_pack(p0, p1));
+              pk[q4 >> 1][(q4 & 1) * 16 + (x >> 1)] = ptx::pack_bf16x2(p0, p1);
+            }
+          float l0, l1;
+          ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
+          return l0 + l1;
+        };
+        auto s_free = [&](float dep) {
+          if constexpr (SINGLE) {  // S may now be overwritten by S(j+1)
+            ptx::tc_fence_before();
+            ptx::mbar_arrive_after(bar(C::B_SFREE + t), dep);
+          }
+        };
+        pv_done = (j == 0);  // PV_t(j-1) known to have completed
+        float l_tile;
+        if (j == 0) {
+          const float m_tile = row_max();
+          s_free(m_tile);
+          if (m_tile > m_ref + kRescaleThreshold) {  // l is still 0
+            m_ref = m_tile;
+          }
+          l_tile = exps(m_ref);
+        } else {
+          // against the current reference: the result stands unless a row maximum grows
+          l_tile = exps(m_ref);
+          const float m_tile = row_max();
+          s_free(m_tile);
+          const bool grow = m_tile > m_ref + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, grow)) {
+            float alpha = 1.0f;
+            if (grow) {
+              alpha = ptx::ex2(m_ref - m_tile);  // 0 when m_ref is still -inf
+              l *= alpha;
+              m_ref = m_tile;
+            }
+            // O_t must hold PV_t(j-1) before it is rescaled in place
+            ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
+            if (!ok) break;
+            pv_done = true;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < D / 32; ++q4) {
+              uint32_t o[32];
+              ptx::tmem_ld32(t_o + q4 * 32, o);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+              ptx::tmem_st32(t_o + q4 * 32, o);
+            }
+            l_tile = exps(m_ref);
+          }
+        }
+        l += l_tile;
+      } else {
+        // row maximum: eight independent 3-input max chains over 16 columns each
+        auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
         float mc[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) {
@@ -580,10 +671,39 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
 #pragma unroll
           for (int x = 2; x < 16; x += 2) mc[a] = ptx::max3(mc[a], col(a, x), col(a, x + 1));
         }
-        return ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * c;
-      };
-      auto exps = [&](float m_now) -> float {
-        const float m_use = (m_now == -INFINITY) ? 0.0f : m_now;
+        const float mx = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+        const float m_tile = mx * c;
+        if constexpr (SINGLE) {  // S may now be overwritten by S(j+1)
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(C::B_SFREE + t));
+        }
+        const bool grow = m_tile > m_ref + kRescaleThreshold;
+        float alpha = 1.0f;
+        if (grow) {
+          alpha = ptx::ex2(m_ref - m_tile);  // 0 when m_ref is still -inf
+          l *= alpha;
+          m_ref = m_tile;
+        }
+        pv_done = (j == 0);  // PV_t(j-1) known to have completed
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_t must hold PV_t(j-1) before it is rescaled in place
+          ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
+          if (!ok) break;
+          pv_done = true;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t o[32];
+            ptx::tmem_ld32(t_o + q4 * 32, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+            ptx::tmem_st32(t_o + q4 * 32, o);
+          }
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+        // p = 2^(s*c - m) for pairs of columns: one packed FMA, two MUFU exp2, one
+        // packed add into one of four running pair-sums, one bf16x2 conversion
         const uint64_t c2 = ptx::f2_pack(c, c);
         const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
         uint64_t part[4] = {0ull, 0ull, 0ull, 0ull};
@@ -600,114 +720,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
           }
         float l0, l1;
         ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
-        return l0 + l1;
-      };
-      auto s_free = [&](float dep) {
-        if constexpr (SINGLE) {  // S may now be overwritten by S(j+1)
-          ptx::tc_fence_before();
-          ptx::mbar_arrive_after(bar(C::B_SFREE + t), dep);
-        }
-      };
-      pv_done = (j == 0);  // PV_t(j-1) known to have completed
-      float l_tile;
-      if (j == 0) {
-        const float m_tile = row_max();
-        s_free(m_tile);
-        if (m_tile > m_ref + kRescaleThreshold) {  // l is still 0
-          m_ref = m_tile;
-        }
-        l_tile = exps(m_ref);
-      } else {
-        // against the current reference: the result stands unless a row maximum grows
-        l_tile = exps(m_ref);
-        const float m_tile = row_max();
-        s_free(m_tile);
-        const bool grow = m_tile > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, grow)) {
-          float alpha = 1.0f;
-          if (grow) {
-            alpha = ptx::ex2(m_ref - m_tile);  // 0 when m_ref is still -inf
-            l *= alpha;
-            m_ref = m_tile;
-          }
-          // O_t must hold PV_t(j-1) before it is rescaled in place
-          ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
-          if (!ok) break;
-          pv_done = true;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) {
-            uint32_t o[32];
-            ptx::tmem_ld32(t_o + q4 * 32, o);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-            ptx::tmem_st32(t_o + q4 * 32, o);
-          }
-          l_tile = exps(m_ref);
-        }
-      }
-      l += l_tile;
-      } else {
-      // row maximum: eight independent 3-input max chains over 16 columns each
-      auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
-      float mc[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        mc[a] = fmaxf(col(a, 0), col(a, 1));
-#pragma unroll
-        for (int x = 2; x < 16; x += 2) mc[a] = ptx::max3(mc[a], col(a, x), col(a, x + 1));
-      }
-      const float mx = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-      const float m_tile = mx * c;
-      if constexpr (SINGLE) {  // S may now be overwritten by S(j+1)
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(C::B_SFREE + t));
-      }
-      const bool grow = m_tile > m_ref + kRescaleThreshold;
-      float alpha = 1.0f;
-      if (grow) {
-        alpha = ptx::ex2(m_ref - m_tile);  // 0 when m_ref is still -inf
-        l *= alpha;
-        m_ref = m_tile;
-      }
-      pv_done = (j == 0);  // PV_t(j-1) known to have completed
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_t must hold PV_t(j-1) before it is rescaled in place
-        ok = __all_sync(0xffffffffu, wait_bar(bar(C::B_ODONE + t), (j - 1) & 1, abort_flag, FAULT_SOFTMAX, wlim));
-        if (!ok) break;
-        pv_done = true;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint32_t o[32];
-          ptx::tmem_ld32(t_o + q4 * 32, o);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          ptx::tmem_st32(t_o + q4 * 32, o);
-        }
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-      // p = 2^(s*c - m) for pairs of columns: one packed FMA, two MUFU exp2, one
-      // packed add into one of four running pair-sums, one bf16x2 conversion
-      const uint64_t c2 = ptx::f2_pack(c, c);
-      const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
-      uint64_t part[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const uint64_t sx = ptx::f2_pack(__uint_as_float(sr[q4][x]), __uint_as_float(sr[q4][x + 1]));
-          float a0, a1;
-          ptx::f2_unpack(ptx::f2_fma(sx, c2, negm2), a0, a1);
-          const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
-          part[q4] = ptx::f2_add(part[q4], ptx::f2_pack(p0, p1));
-          pk[q4 >> 1][(q4 & 1) * 16 + (x >> 1)] = ptx::pack_bf16x2(p0, p1);
-        }
-      float l0, l1;
-      ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
-      l += l0 + l1;
+        l += l0 + l1;
       }
       if (SINGLE && !pv_done) {
         // P is still the A operand of PV(j-1) until that MMA completes
@@ -820,6 +833,12 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
   p.window = a.window;
   p.BH = a.B * a.H;
   p.num_qblocks = (a.n_q + C::ROWS - 1) / C::ROWS;
+  // Without the causal mask every Q tile costs the same, and launching the CTAs of a few
+  // heads together keeps those heads' K and V in L2 (one-tile kernel, same-box A/B with
+  // groups of 8: long cross-attention 4096 x 8192 +1.9 %, unmasked n = 8192 +0.4 %). Causal
+  // launches keep one group (the heaviest tiles of all heads first: grouping cost 1-7 %),
+  // and so does the two-tile d = 128 kernel (grouping cost 0.7-4.5 %).
+  p.head_group = (SINGLE && !LOCAL && !(a.mask_mode & 1) && p.BH > kHeadGroup) ? kHeadGroup : p.BH;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   p.inject_wait_ns = INJECT ? t_inject_wait_ns : kWaitLimitNs;
   p.inject_skip_v_tile = INJECT ? t_inject_skip_v_tile : -1;
