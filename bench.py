@@ -83,17 +83,17 @@ KERNEL_SOURCES = {
     "attn_bwd_tc_kernel": ("attn_bwd.cu", "ptx_sm103.cuh"),
 }
 NCU_TRAFFIC = {
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 152260608,
-    ("long_none_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 115189504,
-    ("long_causal_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 573938688,
-    ("long_none_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 1067328512,
-    ("long_cross_pad_b2_h16_q4096_k8192_d64", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 76296704,
-    ("long_cross_pad_b2_h16_q4096_k8192_d128", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 529853440,
-    ("local_causal_b2_h16_n8192_d64_w511", "attn_fwd_tc_kernel", "8d5f1a1a84c74c6d"): 110792960,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 151273216,
+    ("long_none_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 114921472,
+    ("long_causal_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 571521024,
+    ("long_none_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 1066888448,
+    ("long_cross_pad_b2_h16_q4096_k8192_d64", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 75955712,
+    ("long_cross_pad_b2_h16_q4096_k8192_d128", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 529118208,
+    ("local_causal_b2_h16_n8192_d64_w511", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 110755328,
     # the warp kernel only (the merge kernel is not counted)
-    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "b13c232734a09acc"): 424487936,
+    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "4b397e0815a40523"): 424483072,
     # the fused d = 64 kernel
-    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "865f9a0a58f45e0d"): 291904512,
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "61902fa5aebb4df9"): 291831552,
 }
 
 

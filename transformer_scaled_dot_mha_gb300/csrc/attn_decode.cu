@@ -306,6 +306,8 @@ __device__ __forceinline__ bool stream_chunk(const DecodeParams& p, int bh, int 
 template <int D>
 __global__ void __launch_bounds__(WCfg<D>::WARPS * 32) attn_decode_warp_kernel(const DecodeParams p) {
   using C = WCfg<D>;
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long task = (long long)blockIdx.x * C::WARPS + warp;  // (b*h, chunk)
   if (task >= (long long)p.BH * p.splits) return;
@@ -337,6 +339,8 @@ __global__ void __launch_bounds__(NTHREADS) attn_decode_split_kernel(const Decod
   float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_A);
   auto full = [&](int st) -> uint32_t { return s_base + C::OFF_BAR + 8u * st; };
 
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, bh = blockIdx.y, b = bh / p.H;
   const int n_q = p.n_q;
@@ -534,6 +538,8 @@ __global__ void __launch_bounds__(NTHREADS) attn_decode_split_kernel(const Decod
 // Merge the split ranges of one (b, h): thread x handles output element x of n_q x D.
 template <int D>
 __global__ void __launch_bounds__(NTHREADS) attn_decode_combine_kernel(const DecodeParams p) {
+  ptx::grid_dep_wait();  // the partials of the split kernel
+  ptx::grid_dep_launch();
   const int bh = blockIdx.x;
   const int n_q = p.n_q;
   for (int x = threadIdx.x; x < n_q * D; x += NTHREADS) {
@@ -560,6 +566,25 @@ __global__ void __launch_bounds__(NTHREADS) attn_decode_combine_kernel(const Dec
     if (p.lse && (x % D) == 0)
       p.lse[(size_t)bh * n_q + q] = (L > 0.0f) ? (M + __log2f(L)) * 0.69314718055994530942f : -INFINITY;
   }
+}
+
+// Launches `kernel` on `stream` with programmatic dependent launch allowed: the kernel's
+// CTAs may start while the previous grid on the stream finishes, and wait in
+// grid_dep_wait before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int D>
@@ -590,7 +615,9 @@ int launch_decode(const DecodeArgs& a, float* ws) {
       return ATTN_ERR_CUDA;
     // one warp per (b*h, chunk) task, consecutive chunks of a (b, h) in one CTA
     const unsigned blocks = (unsigned)((bh * p.splits + W::WARPS - 1) / W::WARPS);
-    attn_decode_warp_kernel<D><<<blocks, W::WARPS * 32, W::SMEM_BYTES, a.stream>>>(p);
+    if (launch_pdl(attn_decode_warp_kernel<D>, dim3(blocks), dim3(W::WARPS * 32), W::SMEM_BYTES, a.stream, p) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
   } else {
     void (*split_kernel)(const DecodeParams) = a.n_q <= 2   ? attn_decode_split_kernel<D, 2>
                                                : a.n_q <= 4 ? attn_decode_split_kernel<D, 4>
@@ -599,10 +626,13 @@ int launch_decode(const DecodeArgs& a, float* ws) {
     if (cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
         cudaSuccess)
       return ATTN_ERR_CUDA;
-    split_kernel<<<dim3(p.splits, (unsigned)bh), NTHREADS, C::SMEM_BYTES, a.stream>>>(p);
+    if (launch_pdl(split_kernel, dim3(p.splits, (unsigned)bh), dim3(NTHREADS), C::SMEM_BYTES, a.stream, p) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
   }
   if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  attn_decode_combine_kernel<D><<<(unsigned)bh, NTHREADS, 0, a.stream>>>(p);
+  if (launch_pdl(attn_decode_combine_kernel<D>, dim3((unsigned)bh), dim3(NTHREADS), 0, a.stream, p) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

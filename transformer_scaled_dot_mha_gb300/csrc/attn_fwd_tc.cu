@@ -32,6 +32,10 @@
 // The softmax rescales O only when a row maximum grows by more than 2^8 (a lazy
 // reference maximum); the final O / l is exact whatever reference was used.
 //
+// Launches allow programmatic dependent launch: a CTA initialises its barriers, takes its
+// TMEM and prefetches its tensor maps while the previous grid on the stream finishes,
+// then waits for that grid (griddepcontrol.wait) before its first global access.
+//
 // Every wait on an mbarrier is bounded in time. A wait that runs out records a
 // fault bit (attn_fault_status), raises a CTA-wide abort flag, and every role then
 // stops, waits (bounded) for its own TMA copies or MMAs in flight, frees TMEM and
@@ -231,6 +235,42 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
   const int lane = threadIdx.x & 31;
   const uint64_t wlim = INJECT ? p.inject_wait_ns : kWaitLimitNs;
 
+  // ---- set-up: barriers, TMEM
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(C::B_QFULL), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(bar(C::B_KFULL + s), 1);
+      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);  // one arrival: the issuer that read the stage
+      ptx::mbar_init(bar(C::B_VFULL + s), 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(bar(C::B_SFULL + t), 1);
+      ptx::mbar_init(bar(C::B_SFREE + t), BM);  // every softmax thread arrives
+      ptx::mbar_init(bar(C::B_PFULL + t), BM);
+      ptx::mbar_init(bar(C::B_ODONE + t), 1);
+    }
+    for (int x = 0; x < 4; ++x) ptx::mbar_init(bar(C::B_DRAIN + x), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == C::WARP_MMA0) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == C::WARP_LOAD && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // set-up above overlaps the previous grid's tail; every global access comes after this
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+
   // ---- which C::ROWS query rows of which (b, h): groups of p.head_group heads one after
   // the other, within a group the heaviest causal blocks first with its heads interleaved
   int bh, qb;
@@ -273,38 +313,6 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
   const int n_max = max(jb0 + n_t0, jb1 + n_t1) - J0;
   const int off1 = jb1 - J0;  // ring use of tile 1's first K/V tile
 
-  // ---- set-up: barriers, TMEM
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(bar(C::B_QFULL), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
-      ptx::mbar_init(bar(C::B_KFULL + s), 1);
-      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);  // one arrival: the issuer that read the stage
-      ptx::mbar_init(bar(C::B_VFULL + s), 1);
-      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
-    }
-    for (int t = 0; t < 2; ++t) {
-      ptx::mbar_init(bar(C::B_SFULL + t), 1);
-      ptx::mbar_init(bar(C::B_SFREE + t), BM);  // every softmax thread arrives
-      ptx::mbar_init(bar(C::B_PFULL + t), BM);
-      ptx::mbar_init(bar(C::B_ODONE + t), 1);
-    }
-    for (int x = 0; x < 4; ++x) ptx::mbar_init(bar(C::B_DRAIN + x), 1);
-    *abort_flag = 0;
-    ptx::fence_mbar_init();
-  }
-  if (warp == C::WARP_MMA0) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
-    ptx::tmem_relinquish();
-  }
-  if (warp == C::WARP_LOAD && lane == 0) {
-    ptx::prefetch_tmap(&tm_q);
-    ptx::prefetch_tmap(&tm_k);
-    ptx::prefetch_tmap(&tm_v);
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp >= C::SOFTMAX_WARPS) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CONTROL));
@@ -844,8 +852,19 @@ int launch_variant(const TcArgs& a, const CUtensorMap& mq, const CUtensorMap& mk
   p.inject_skip_v_tile = INJECT ? t_inject_skip_v_tile : -1;
   const long long grid = (long long)p.BH * p.num_qblocks;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE, INJECT>
-      <<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_fwd_tc_kernel<D, LOCAL, HEADS_INTERLEAVED, SINGLE, INJECT>, mq, mk, mv, p) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -194,6 +194,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if constexpr (CL > 1) ptx::cluster_sync();  // the peer's barriers exist before any multicast
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  ptx::grid_dep_wait();  // X may be the previous grid's output
+  ptx::grid_dep_launch();
   const int rank = CL > 1 ? (int)ptx::cluster_ctarank() : 0;
   const int unit0 = (int)(blockIdx.x / CL), units_step = (int)(gridDim.x / CL);
   constexpr uint16_t kPeers = (uint16_t)((1u << CL) - 1);
@@ -459,13 +461,15 @@ int launch_linear_cl(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cud
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = CL;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, attn_linear_kernel<CL>, mx[0], mw[0], my[0], mx[1], mw[1], my[1], mx[2], mw[2], my[2],
                          p) != cudaSuccess)
     return ATTN_ERR_CUDA;

@@ -11,6 +11,8 @@
 // kernel, and the output projection. split_heads and the concatenation cost no
 // copies: the attention kernel reads Q', K', V' and writes A in their [B, n, h*d]
 // layout through its heads-interleaved tensor maps (head i = columns i*d .. i*d+d-1).
+// All three allow programmatic dependent launch, so each one's set-up (barriers, TMEM,
+// tensor maps) overlaps the end of the one before it.
 #include <cuda_runtime.h>
 
 #include <cstdint>

@@ -218,6 +218,13 @@ __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
                : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Waits until the grids this one was launched to overlap (programmatic dependent launch)
+// have completed and their memory writes are visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid on the stream start launching; its CTAs still stop at grid_dep_wait.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
