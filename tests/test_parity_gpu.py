@@ -273,3 +273,27 @@ def test_bf16_multi_wave_grid(orc, mode, n_q, n_k):
     out, lse = run_bf16(q, k, v, kl, w.scale, mode)
     ref, ref_lse = orc.attention(q, k, v, w.scale, mode, kl)
     assert_bf16_close(out, lse, ref, ref_lse)
+
+
+def test_bf16_dependent_calls_on_one_stream(orc):
+    """Kernels of this library start before the previous kernel on the stream has
+    finished (programmatic dependent launch) and wait for it before touching memory.
+    Chain them so that each reads what the one before wrote: O1 = Attn(Q, K, V), then
+    O2 = Attn(O1, K, V) with no synchronisation in between, several times over. Both
+    against the oracle, O2 computed from the oracle's own inputs: the bf16 O1 the GPU
+    returned."""
+    w, (q, k, v, _) = gen("decoder_causal_b16_h8_n512_d64", seed=5200, B=2, H=4, n_q=640, n_k=640)
+    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    o1, o2 = torch.empty_like(qd), torch.empty_like(qd)
+    for _ in range(5):
+        o1.fill_(float("nan"))
+        o2.fill_(float("nan"))
+        attn.attn_fwd(qd, kd, vd, o1, None, w.scale, C, None)
+        attn.attn_fwd(o1, kd, vd, o2, None, w.scale, C, None)
+    torch.cuda.synchronize()
+    o1_bits = o1.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref1, _ = orc.attention(q, k, v, w.scale, C)
+    ref2, _ = orc.attention(o1_bits, k, v, w.scale, C)
+    for out, ref in ((o1, ref1), (o2, ref2)):
+        err = np.abs(bf16_to_f64(out) - ref)
+        assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN
