@@ -176,6 +176,40 @@ def test_bf16_large_scores_rescaling(orc):
     assert np.abs(lse - ref_lse).max() <= LSE_TOL
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mode", [0, C])
+def test_bf16_score_jumps_within_later_tiles(orc, d, mode):
+    """Keys whose scores jump well above everything before them, placed in the first
+    and the second 64-key half of later 128-key tiles (and in both halves of one tile),
+    plus a cluster of keys that raises a half's sum of weights without raising its row
+    maximum past the rescaling threshold: every way in which the running maximum of a
+    row can be overtaken after the first tile, against the oracle."""
+    n = 1024
+    name = "long_none_b2_h16_n8192_d64" if d == 64 else "long_none_b2_h16_n8192_d128"
+    w, (q, k, v, kl) = gen(name, seed=4150 + d + mode, B=1, H=2, n_q=n, n_k=n)
+    rng = np.random.Generator(np.random.PCG64(4160 + d))
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    qf, kf = oracle.widen(q), oracle.widen(k)
+    qf += 4.0 * u  # every query leans on u, so a key along u raises every row's score
+    # (key, jump of its score in log2 units): after the first tile the reference maximum
+    # sits a few units above the typical score, and rescaling starts 8 units above it
+    jumps = [(130, 10), (131, 10), (132, 10), (133, 10),  # tile 1, first half: sum only
+             (340, 20),                                   # tile 2, second half
+             (520, 30), (600, 40),                        # tile 4, both halves
+             (800, 26), (1000, 46)]                       # tile 6 below, tile 7 above
+    for key, jump in jumps:
+        kf[:, :, key, :] += jump * math.log(2.0) / (4.0 * w.scale) * u
+    q2, k2 = W.to_bf16_bits(qf.astype(np.float32)), W.to_bf16_bits(kf.astype(np.float32))
+    out, lse = run_bf16(q2, k2, v, kl, w.scale, mode)
+    ref, ref_lse = orc.attention(q2, k2, v, w.scale, mode)
+    # sharp rows: the bound of the rescaling test above (2 * 2^-8 max|V|)
+    err = np.abs(out - ref)
+    assert np.isfinite(out).all()
+    assert err.max() <= 2.0 ** -7 * np.abs(oracle.widen(v)).max() and err.mean() <= BF16_MEAN
+    assert np.abs(lse - ref_lse).max() <= LSE_TOL
+
+
 def test_bf16_guard_bands_and_determinism():
     """Nothing is written outside out / lse, and two calls give identical bits."""
     w, (q, k, v, kl) = gen("cross_pad_b16_h16_q256_k512_d64", seed=4200, B=2, H=2, n_q=257, n_k=300)

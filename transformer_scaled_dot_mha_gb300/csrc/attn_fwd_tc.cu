@@ -558,6 +558,10 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) ptx::tmem_ld32(t_s + q4 * 32, sr[q4]);
       ptx::tmem_wait_ld();
+      if constexpr (SINGLE && !LOCAL) {  // S is in registers: S(j+1) may overwrite it now
+        ptx::tc_fence_before();
+        ptx::mbar_arrive_after(bar(C::B_SFREE + t), __uint_as_float(sr[3][31]));
+      }  // (the maximum-first paths release S once the maximum is formed)
 
       // mask: key-length boundary, the causal diagonal, the local window
       const int j0 = (jb + j) * BN;
@@ -585,12 +589,14 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       uint32_t pk[2][32];
       if constexpr (SINGLE && !LOCAL) {
         // d = 64: after the first tile the exponentials are taken against the current
-        // reference maximum while the tile's maximum is formed beside them (the two are
-        // independent); only a row whose maximum grows past the threshold (rare after
-        // the first tile) redoes them against the new reference. Same results bit for
-        // bit; the maximum leaves the per-tile dependency chain. At d = 128 (the softmax
-        // warps' registers run out) and with a local window (-6 %) this measured slower,
-        // so those paths keep the order maximum -> exponentials.
+        // reference maximum, before the tile's maximum is known. Every term of the
+        // tile's sum bounds itself, so a sum of at most 2^7 shows that no score exceeds
+        // the reference by the rescaling threshold (2^8); only a larger sum (rare after
+        // the first tile) needs the exact maximum, and only a row whose maximum did grow
+        // past the threshold redoes the exponentials against the new reference. Same
+        // results bit for bit as maximum -> exponentials, with the maximum out of the
+        // per-tile work. At d = 128 (the softmax warps' registers run out) and with a
+        // local window (-6 %) this measured slower, so those paths keep that order.
         // row maximum: eight independent 3-input max chains over 16 columns each
         auto col = [&](int a, int x) { return __uint_as_float(sr[a >> 1][(a & 1) * 16 + x]); };
         auto row_max = [&]() -> float {
@@ -623,17 +629,10 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
           ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), l0, l1);
           return l0 + l1;
         };
-        auto s_free = [&](float dep) {
-          if constexpr (SINGLE) {  // S may now be overwritten by S(j+1)
-            ptx::tc_fence_before();
-            ptx::mbar_arrive_after(bar(C::B_SFREE + t), dep);
-          }
-        };
         pv_done = (j == 0);  // PV_t(j-1) known to have completed
         float l_tile;
         if (j == 0) {
           const float m_tile = row_max();
-          s_free(m_tile);
           if (m_tile > m_ref + kRescaleThreshold) {  // l is still 0
             m_ref = m_tile;
           }
@@ -641,9 +640,14 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
         } else {
           // against the current reference: the result stands unless a row maximum grows
           l_tile = exps(m_ref);
-          const float m_tile = row_max();
-          s_free(m_tile);
-          const bool grow = m_tile > m_ref + kRescaleThreshold;
+          // a sum of at most 2^7: no score of the tile exceeds m_ref + 7 (a NaN sum or
+          // a reference still at -inf take the exact test)
+          float m_tile = m_ref;
+          bool grow = false;
+          if (__any_sync(0xffffffffu, !(l_tile <= 128.0f) || m_ref == -INFINITY)) {
+            m_tile = row_max();
+            grow = m_tile > m_ref + kRescaleThreshold;
+          }
           if (__any_sync(0xffffffffu, grow)) {
             float alpha = 1.0f;
             if (grow) {
