@@ -148,12 +148,15 @@ struct Params {
 
 // Bounded wait on an mbarrier phase. Returns false (after recording `who`) if the
 // phase did not complete within limit_ns, or if another role already aborted.
+// sleepy: retry with a 1 us suspend-time hint (the control warps of the d = 64 kernel:
+// +0.9 % on the long shapes; the softmax warps' waits are short, and at d = 128 the one
+// MMA issuer is better off polling, -1.3 % with the hint).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t who,
-                                         uint64_t limit_ns) {
+                                         uint64_t limit_ns, bool sleepy = false) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (sleepy ? ptx::mbar_try_wait_sleep(bar, parity, 1000u) : ptx::mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > limit_ns) {
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       for (int j = 0; j < n_max && ok; ++j) {
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
-        ok = wait_bar(bar(C::B_KEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER, wlim);
+        ok = wait_bar(bar(C::B_KEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER, wlim, SINGLE);
         if (!ok) break;
         ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c)
@@ -345,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
             break;
           }
         }
-        ok = wait_bar(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER, wlim);
+        ok = wait_bar(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, FAULT_PRODUCER, wlim, SINGLE);
         if (!ok) {
           issued = 2 * j + 1;
           break;
@@ -374,10 +377,10 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
     const int role = warp - C::WARP_MMA0;
     if (SINGLE && role == 0 && lane == 0 && n_t0 > 0) {
       // S(j) = Q K_j^T, as soon as K_j has landed and the softmax has loaded S(j-1)
-      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA, wlim);
+      bool ok = wait_bar(bar(C::B_QFULL), 0, abort_flag, FAULT_MMA, wlim, true);
       for (int j = 0; j < n_t0 && ok; ++j) {
-        ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim) &&
-             (j == 0 || wait_bar(bar(C::B_SFREE), (j - 1) & 1, abort_flag, FAULT_MMA, wlim));
+        ok = wait_bar(bar(C::B_KFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim, true) &&
+             (j == 0 || wait_bar(bar(C::B_SFREE), (j - 1) & 1, abort_flag, FAULT_MMA, wlim, true));
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t k_stage = s_k + (j % C::STAGES) * C::TILE_BYTES;
@@ -402,8 +405,8 @@ __global__ void __launch_bounds__(Cfg<D, SINGLE>::THREADS, Cfg<D, SINGLE>::CTAS_
       const uint32_t d_o = tmem + C::TMEM_O;
       bool ok = true;
       for (int j = 0; j < n_t0 && ok; ++j) {
-        ok = wait_bar(bar(C::B_PFULL), j & 1, abort_flag, FAULT_MMA, wlim) &&
-             wait_bar(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim);
+        ok = wait_bar(bar(C::B_PFULL), j & 1, abort_flag, FAULT_MMA, wlim, true) &&
+             wait_bar(bar(C::B_VFULL + j % C::STAGES), (j / C::STAGES) & 1, abort_flag, FAULT_MMA, wlim, true);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t v_stage = s_v + (j % C::STAGES) * C::TILE_BYTES;
