@@ -83,17 +83,17 @@ KERNEL_SOURCES = {
     "attn_bwd_tc_kernel": ("attn_bwd.cu", "ptx_sm103.cuh"),
 }
 NCU_TRAFFIC = {
-    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 151273216,
-    ("long_none_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 114921472,
-    ("long_causal_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 571521024,
-    ("long_none_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 1066888448,
-    ("long_cross_pad_b2_h16_q4096_k8192_d64", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 75955712,
-    ("long_cross_pad_b2_h16_q4096_k8192_d128", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 529118208,
-    ("local_causal_b2_h16_n8192_d64_w511", "attn_fwd_tc_kernel", "7da00165d2ef943e"): 110755328,
+    ("long_causal_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "dd287655676f270e"): 153654016,
+    ("long_none_b2_h16_n8192_d64", "attn_fwd_tc_kernel", "dd287655676f270e"): 114852352,
+    ("long_causal_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "dd287655676f270e"): 572768256,
+    ("long_none_b2_h16_n8192_d128", "attn_fwd_tc_kernel", "dd287655676f270e"): 1066685952,
+    ("long_cross_pad_b2_h16_q4096_k8192_d64", "attn_fwd_tc_kernel", "dd287655676f270e"): 76273152,
+    ("long_cross_pad_b2_h16_q4096_k8192_d128", "attn_fwd_tc_kernel", "dd287655676f270e"): 529536512,
+    ("local_causal_b2_h16_n8192_d64_w511", "attn_fwd_tc_kernel", "dd287655676f270e"): 110697472,
     # the warp kernel only (the merge kernel is not counted)
-    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "4b397e0815a40523"): 424483072,
+    ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "15a9265a513b2001"): 424486400,
     # the fused d = 64 kernel
-    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "61902fa5aebb4df9"): 291831552,
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "caee004531853f22"): 291833088,
 }
 
 
