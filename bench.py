@@ -652,6 +652,78 @@ def cpu_baseline_mha(w, target_s=12.0):
                       f"fp64 C oracle (projections single-threaded, attention on {threads} threads), {dt:.2f} s wall"}
 
 
+def run_ours_weights(args, w):
+    """attn_weights: the softmax weight matrix [B, h, n_q, n_k] (fp32) from q, k and the
+    forward's lse. HBM-bound on its write; value = algorithmic bytes per second."""
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from transformer_scaled_dot_mha_gb300 import attn
+
+    attn.lib()
+    q, k, v, kl = W.make_inputs(w, shard_seed(w, rank))
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    kld = torch.from_numpy(kl).to(dev)
+    key_lens = kld if w.mask_mode & W.MASK_KEY_PADDING else None
+    out = torch.empty((w.B, w.H, w.n_q, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.n_q), dtype=torch.float32, device=dev)
+    attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens)
+    wts = torch.empty((w.B, w.H, w.n_q, w.n_k), dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        attn.attn_weights(qd, kd, lse, wts, w.scale, w.mask_mode, key_lens, stream)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for e0, e1 in evs:
+        flush()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    st, code = attn.attn_fault_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"kernel fault record {code:#x} in the timed region")
+    total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    ms = total_ms / args.steps
+    nbytes = w.B * w.H * (w.n_q * w.n_k * 4 + (w.n_q + w.n_k) * w.d_k * 2 + w.n_q * 4)
+    peaks, peak_src = load_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+            "peak_source": f"hbm_gbs of {peak_src}", "kernel": "attn_weights_kernel", "algorithmic_bytes": nbytes,
+            "frac": round(achieved / float(peaks["hbm_gbs"]), 4), "traffic": None}
+    return {
+        "metric": "attention weights (softmax matrix) GB/s on 1 GB300 and % of measured HBM bandwidth",
+        "value": round(achieved, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, {"l2": L2_NOTE, "pass": "attn_weights (fp32 weights from q, k and lse)",
+                                "parallelism": "single GPU"}),
+        "roofline": roof,
+        "e2e": None,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+
+
 def run_ours_mha(args, w):
     import torch
 
@@ -828,6 +900,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--grad", action="store_true", help="time the gradients (attn_bwd) instead of the forward")
     ap.add_argument("--mha", action="store_true", help="time the multi-head layer (attn_mha_fwd) instead")
+    ap.add_argument("--weights", action="store_true",
+                    help="time attn_weights (the fp32 softmax weight matrix) instead of the forward")
     ap.add_argument("--warm-l2", dest="warm_l2", action="store_true",
                     help="forward only: no L2 flush between timed steps, so a workload that fits in L2 is "
                          "read from it (the tensor-roofline view of a short shape; not the default line)")
@@ -841,7 +915,11 @@ def main():
     if world != args.gpus:
         if world == 1 and args.gpus > 1:
             ap.error("--gpus N > 1 must be launched with torchrun (one process per GPU)")
-    if args.mha:
+    if args.weights:
+        if args.mha or args.grad or args.impl == "reference" or w.mask_mode & (W.MASK_DECODE | W.MASK_WINDOW):
+            ap.error("--weights times attn_weights alone (--impl ours) on the full-attention workloads")
+        line = run_ours_weights(args, w)
+    elif args.mha:
         if args.grad or w.mask_mode & (W.MASK_DECODE | W.MASK_WINDOW):
             ap.error("--mha covers the forward of the full-attention workloads")
         if args.impl == "reference":

@@ -83,6 +83,28 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
              int mask_mode, const int32_t* key_lens, void* stream);
 
 /*
+ * attn_weights -- the softmax weights of Eq. (1) themselves (rockcohen.cc "Attention Is
+ * All You Need" section 5.1), the second value the pages' scaled_dot_product_attention
+ * returns beside the output (csdn blog reimplementation, scaled_dot_product_attention):
+ *   w[b, h, i, j] = exp(scale * q_i . k_j - lse_i) for every legal key j of row i
+ *   (the mask of attn_fwd), and exactly 0 for the others and for every key of a row
+ *   with no legal key (lse_i = -inf).
+ * With lse the log-sum-exp that attn_fwd returned for the same q, k, scale, mask_mode
+ * and key_lens, each row of legal weights sums to 1 up to that lse's rounding.
+ *   q [B, h, n_q, d], k [B, h, n_k, d]: bf16 device arrays, 16-byte aligned.
+ *   lse [B, h, n_q]: float32 device array (required).
+ *   w [B, h, n_q, n_k]: float32 device array, 16-byte aligned, written in full;
+ *           B*h*n_q*n_k floats, owned by the caller.
+ *   mask_mode, key_lens, scale and stream as in attn_fwd.
+ * Supported: d in {64, 128}; otherwise ATTN_ERR_UNSUPPORTED. The score q_i . k_j
+ * accumulates in fp32 on the tensor cores; the exponential is exp2 of the scaled score
+ * in log2 units. The matrix is B*h*n_q*n_k floats: this is for inspecting attention
+ * (the forward never forms it), and its cost is that write.
+ */
+int attn_weights(const void* q, const void* k, const float* lse, float* w, int B, int h, int n_q, int n_k, int d,
+                 float scale, int mask_mode, const int32_t* key_lens, void* stream);
+
+/*
  * attn_fwd_host_workspace_size -- bytes of device workspace attn_fwd_host needs for
  * this shape and mask (four chunk slots of Q, K, V, out, lse plus the key lengths;
  * the mask enters through the chunk plan). Returns 0 for an invalid shape or mask
@@ -343,7 +365,7 @@ int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void*
  * issuer, bit 2 softmax, bit 3 epilogue (attn_fwd), bit 4 decode copy (attn_decode),
  * bit 5 gradient kernels (attn_bwd), bit 6 attn_fwd found its shared memory not
  * 1024-byte aligned (it then writes nothing), bit 7 projection kernel (attn_linear,
- * attn_mha_fwd).
+ * attn_mha_fwd), bit 8 attn_weights.
  */
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code);
 

@@ -218,3 +218,20 @@ def test_host_gradients_workspace_and_argument_checks(L):
     assert call(n_k=200) == attn.ATTN_ERR_INVALID              # causal needs n_q == n_k
     assert call(mask=2) == attn.ATTN_ERR_INVALID               # key padding without key_lens
     assert call(d_k=96, d_v=96) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_weights_argument_checks(L):
+    """attn_weights rejects bad arguments before touching the device (no GPU needed)."""
+    ok = dict(q=16, k=32, lse=48, w=64, B=1, h=1, n_q=8, n_k=8, d=64, scale=0.125, mask_mode=0, key_lens=None)
+
+    def cw(**kw):
+        a = dict(ok, **kw)
+        return L.attn_weights(a["q"], a["k"], a["lse"], a["w"], a["B"], a["h"], a["n_q"], a["n_k"], a["d"],
+                              a["scale"], a["mask_mode"], a["key_lens"], None)
+
+    for bad in (dict(q=None), dict(k=None), dict(lse=None), dict(w=None), dict(B=0), dict(n_k=0),
+                dict(scale=float("nan")), dict(mask_mode=4), dict(mask_mode=1, n_k=9), dict(mask_mode=2),
+                dict(w=72), dict(q=8), dict(lse=50), dict(B=1 << 20, h=1 << 10, n_q=1 << 16, n_k=1 << 16)):
+        assert cw(**bad) == attn.ATTN_ERR_INVALID, bad
+    assert cw(d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert cw(d=32) == attn.ATTN_ERR_UNSUPPORTED

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp,
                                     ctypes.c_size_t, vp]
         L.attn_bwd_host.restype = i
+        L.attn_weights.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]
+        L.attn_weights.restype = i
         L.attn_linear.argtypes = [vp, vp, vp, vp, i, i, i, vp]
         L.attn_linear.restype = i
         L.attn_mha_workspace_size.argtypes = [i, i, i, i, i, i]
@@ -361,6 +363,28 @@ def attn_mha_fwd(x_q, x_kv, w_q, w_k, w_v, w_o, out, H, workspace, b_q=None, b_k
     if st != ATTN_OK:
         raise AttnError(st, "attn_mha_fwd")
     return out
+
+
+def attn_weights(q, k, lse, w, scale=None, mask_mode=MASK_NONE, key_lens=None, stream=None):
+    """The softmax weights ``w [B, H, n_q, n_k]`` (float32, caller-provided) of bf16
+    ``q``, ``k`` given the ``lse`` attn_fwd returned for the same inputs and mask."""
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16)
+    _check(lse, "lse", torch.float32, 3)
+    _check(w, "w", torch.float32)
+    B, H, n_q, d = q.shape
+    n_k = k.shape[2]
+    if k.shape != (B, H, n_k, d) or lse.shape != (B, H, n_q) or w.shape != (B, H, n_q, n_k):
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} lse{tuple(lse.shape)} w{tuple(w.shape)}")
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, 1)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_weights(_ptr(q), _ptr(k), _ptr(lse), _ptr(w), B, H, n_q, n_k, d, float(scale), int(mask_mode),
+                            _ptr(key_lens), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_weights")
+    return w
 
 
 def attn_linear(x, w, y, bias=None, stream=None):

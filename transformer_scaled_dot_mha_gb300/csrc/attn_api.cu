@@ -61,6 +61,20 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   return attn::launch_attn_tc(a, enc);
 }
 
+int attn_weights(const void* q, const void* k, const float* lse, float* w, int B, int h, int n_q, int n_k, int d,
+                 float scale, int mask_mode, const int32_t* key_lens, void* stream) {
+  int st = check_common(q, k, k, w, lse, B, h, n_q, n_k, d, d, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (!lse || !aligned(q, 16) || !aligned(k, 16) || !aligned(w, 16)) return ATTN_ERR_INVALID;
+  // the weights tensor itself must stay addressable with 64-bit element offsets
+  if ((long long)B * h * n_q > (1LL << 62) / n_k) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::WeightsArgs a{q, k, lse, w, B, h, n_q, n_k, d, scale, mask_mode, key_lens, static_cast<cudaStream_t>(stream)};
+  return attn::launch_attn_weights(a, enc);
+}
+
 size_t attn_fwd_host_workspace_size(int B, int h, int n_q, int n_k, int d, int mask_mode) {
   if (B <= 0 || h <= 0 || n_q <= 0 || n_k <= 0 || (d != 64 && d != 128)) return 0;
   if (mask_mode < 0 || mask_mode > (ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return 0;
@@ -245,12 +259,12 @@ int attn_mha_fwd(const void* x_q, const void* x_kv, const void* w_q, const void*
 }
 
 int attn_fault_status(void* stream, int clear, uint32_t* fault_code) {
-  uint32_t w = 0, wb = 0, wl = 0;
+  uint32_t w = 0, wb = 0, wl = 0, ww = 0;
   const int st = attn::read_fault_word(static_cast<cudaStream_t>(stream), clear, &w);
   if (st == ATTN_ERR_CUDA || attn::read_bwd_fault_word(clear, &wb) != ATTN_OK ||
-      attn::read_linear_fault_word(clear, &wl) != ATTN_OK)
+      attn::read_linear_fault_word(clear, &wl) != ATTN_OK || attn::read_weights_fault_word(clear, &ww) != ATTN_OK)
     return ATTN_ERR_CUDA;
-  w |= wb | wl;
+  w |= wb | wl | ww;
   if (fault_code) *fault_code = w;
   return w ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }

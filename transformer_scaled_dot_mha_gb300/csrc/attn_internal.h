@@ -31,6 +31,19 @@ struct TcArgs {
   int heads_interleaved = 0;  // 1: q, k, v, out are [B, n, H*d] instead of [B, H, n, d]
 };
 
+// Validated arguments of one attn_weights call.
+struct WeightsArgs {
+  const void* q;
+  const void* k;
+  const float* lse;
+  float* w;
+  int B, H, n_q, n_k, d;
+  float scale;
+  int mask_mode;
+  const int32_t* key_lens;
+  cudaStream_t stream;
+};
+
 // Validated arguments of one fp32 call.
 struct F32Args {
   const float* q;
@@ -124,6 +137,8 @@ int launch_attn_bwd_host(const BwdArgs& a, PFN_encodeTiled enc, void* workspace)
 int read_bwd_fault_word(int clear, uint32_t* out);                       // attn_bwd.cu
 int launch_linear(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cudaStream_t stream);  // attn_linear.cu
 int read_linear_fault_word(int clear, uint32_t* out);                    // attn_linear.cu
+int launch_attn_weights(const WeightsArgs& a, PFN_encodeTiled enc);     // attn_weights.cu
+int read_weights_fault_word(int clear, uint32_t* out);                   // attn_weights.cu
 size_t mha_workspace_bytes(int B, int n_q, int n_k, int H, int d);         // attn_mha.cu
 int launch_attn_mha(const MhaArgs& a, PFN_encodeTiled enc, void* workspace);  // attn_mha.cu
 // Host-operand pipelines (attn_host.cu, attn_bwd_host.cu): chunks of the flattened
