@@ -474,10 +474,15 @@ def cpu_baseline_grad(w, inputs, dout):
     hs = max(1, min(threads, w.H))
     sl = lambda a: np.ascontiguousarray(a[:1, :hs])
     kl1 = kl[:1] if w.mask_mode & W.MASK_KEY_PADDING else None
+    window = w.window if w.mask_mode & W.MASK_WINDOW else 0
     t0 = time.perf_counter()
-    orc.attention_bwd(sl(q), sl(k), sl(v), sl(dout), w.scale, w.mask_mode, kl1, n_threads=hs)
+    orc.attention_bwd(sl(q), sl(k), sl(v), sl(dout), w.scale, w.mask_mode, kl1, window=window, n_threads=hs)
     dt = time.perf_counter() - t0
-    flops = 2.0 * (3 * w.d_k + 2 * w.d_v) * W.legal_pairs(1, hs, w.n_q, w.n_k, w.mask_mode, kl1)
+    if w.mask_mode & W.MASK_WINDOW:
+        pairs = W.legal_pairs_window(1, hs, w.n_q, w.mask_mode, w.window, kl1)
+    else:
+        pairs = W.legal_pairs(1, hs, w.n_q, w.n_k, w.mask_mode, kl1)
+    flops = 2.0 * (3 * w.d_k + 2 * w.d_v) * pairs
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": hs, "kind": "oracle",
             "sample": f"{hs} whole heads (batch 0) of the workload, fp64 C oracle gradients, {dt:.2f} s wall"}
 
@@ -504,14 +509,23 @@ def run_ours_grad(args, w):
     key_lens = kld if w.mask_mode & W.MASK_KEY_PADDING else None
     out = torch.empty((w.B, w.H, w.n_q, w.d_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, w.n_q), dtype=torch.float32, device=dev)
-    attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens)
+    local_window = bool(w.mask_mode & W.MASK_WINDOW)
+    base_mask = w.mask_mode & ~W.MASK_WINDOW
+    if local_window:
+        attn.attn_fwd_local(qd, kd, vd, out, w.window, lse, w.scale, base_mask, key_lens)
+    else:
+        attn.attn_fwd(qd, kd, vd, out, lse, w.scale, w.mask_mode, key_lens)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     ws = torch.empty(attn.attn_bwd_workspace_size(w.B, w.H, w.n_q, w.d_k), dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        attn.attn_bwd(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, w.scale, w.mask_mode, key_lens, stream)
+        if local_window:
+            attn.attn_bwd_local(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, w.window, w.scale, base_mask, key_lens,
+                                stream)
+        else:
+            attn.attn_bwd(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, w.scale, w.mask_mode, key_lens, stream)
 
     for _ in range(args.warmup):
         flush()
@@ -553,12 +567,24 @@ def run_ours_grad(args, w):
     grads_h = [torch.empty_like(t, device="cpu").pin_memory() for t in (dq, dk, dv)]
     e2e_steps = max(3, min(args.steps, 20))
 
-    hws = torch.empty(attn.attn_bwd_host_workspace_size(w.B, w.H, w.n_q, w.n_k, w.d_k, w.mask_mode),
-                      dtype=torch.uint8, device=dev)
+    if local_window:  # copies around attn_bwd_local on one stream
+        devs = (qd, kd, vd, out, gd, lse)
 
-    def e2e_step():
-        attn.attn_bwd_host(*hosts[:5], hosts[5], *grads_h, hws, w.scale, w.mask_mode,
-                           klh if key_lens is not None else None, stream)
+        def e2e_step():
+            for dst, src in zip(devs, hosts):
+                dst.copy_(src, non_blocking=True)
+            if key_lens is not None:
+                kld.copy_(klh, non_blocking=True)
+            step()
+            for dst, src in zip(grads_h, (dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+    else:
+        hws = torch.empty(attn.attn_bwd_host_workspace_size(w.B, w.H, w.n_q, w.n_k, w.d_k, w.mask_mode),
+                          dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            attn.attn_bwd_host(*hosts[:5], hosts[5], *grads_h, hws, w.scale, w.mask_mode,
+                               klh if key_lens is not None else None, stream)
 
     for _ in range(3):
         e2e_step()
@@ -575,7 +601,9 @@ def run_ours_grad(args, w):
     e2e = {"value": round(weak_scaling_tflops(flops_step, 1, e2e_ms, world), 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
            "steps": e2e_steps,
-           "how": ("attn_bwd_host on pinned host buffers: chunked H2D / gradient kernels / D2H overlapped on the "
+           "how": ("pinned host buffers copied in, attn_bwd_local, gradients copied out, one stream"
+                   if local_window else
+                   "attn_bwd_host on pinned host buffers: chunked H2D / gradient kernels / D2H overlapped on the "
                    "library's streams, CUDA events on the caller's stream")}
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -598,7 +626,7 @@ def run_ours_grad(args, w):
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, {"pass": "gradients (attn_bwd)",
+        "config": config_of(w, {"pass": "gradients (attn_bwd_local)" if local_window else "gradients (attn_bwd)",
                                 "schedule": ("fused: five products once, dQ by TMA reduce-add" if fused else
                                              "deterministic: dK/dV kernel + dQ kernel, seven products"),
                                 "flops": "algorithmic: 2*(3*d_k+2*d_v) per legal (query, key) pair",
@@ -926,8 +954,8 @@ def main():
             ap.error("--mha is measured for --impl ours; its line carries the oracle's cpu_baseline")
         line = run_ours_mha(args, w)
     elif args.grad:
-        if w.mask_mode & (W.MASK_DECODE | W.MASK_WINDOW):
-            ap.error("--grad covers the full-attention workloads (no decode or local-window masks)")
+        if w.mask_mode & W.MASK_DECODE:
+            ap.error("--grad covers the full-attention and local-window workloads (no decode)")
         if args.impl == "reference":
             ap.error("--grad is measured for --impl ours; its line carries the oracle's cpu_baseline")
         line = run_ours_grad(args, w)

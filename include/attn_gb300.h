@@ -274,6 +274,22 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              void* stream);
 
 /*
+ * attn_bwd_local -- gradients of attn_fwd_local (restricted self-attention: key j is
+ * legal for query i only if |i - j| <= window, together with mask_mode; SURVEY's f4
+ * row, vlmlib.cn "restricted self-attention"), exactly as attn_bwd computes them for
+ * attn_fwd: the same definitions, numerics, schedules, flags and workspace
+ * (attn_bwd_workspace_size(B, h, n, d_k, flags)), with n_q = n_k = n and the window
+ * entering P's mask. out and lse are those attn_fwd_local returned for the same
+ * q, k, v, scale, window, mask_mode and key_lens. window < 0: ATTN_ERR_INVALID.
+ * Key tiles no query of a query tile may see, and query tiles outside a key tile's
+ * window, are skipped; every dq, dk, dv element is still written.
+ */
+int attn_bwd_local(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int h, int n, int d_k, int d_v,
+                   float scale, int window, int mask_mode, const int32_t* key_lens, int flags, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_host_workspace_size -- bytes of device workspace attn_bwd_host needs for
  * this shape, head size, mask and flags (four chunk slots of the nine per-head tensors
  * and their gradient workspace, plus the key lengths). Returns 0 for an invalid shape,

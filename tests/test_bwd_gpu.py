@@ -75,28 +75,36 @@ def draw(seed, B, H, n_q, n_k, d, mask, lens=None):
     return q, k, v, dout, np.asarray(lens, np.int32)
 
 
-def run_bwd(q, k, v, dout, scale, mask, lens, flags=0):
+def run_bwd(q, k, v, dout, scale, mask, lens, flags=0, window=None):
+    """attn_fwd + attn_bwd, or with a window attn_fwd_local + attn_bwd_local."""
     B, H, n_q, d = q.shape
     qd, kd, vd, gd = dev_bf16(q), dev_bf16(k), dev_bf16(v), dev_bf16(dout)
     kl = torch.from_numpy(lens).cuda() if mask & W.MASK_KEY_PADDING else None
     out = torch.empty_like(qd)
     lse = torch.empty((B, H, n_q), dtype=torch.float32, device="cuda")
-    attn.attn_fwd(qd, kd, vd, out, lse, scale, mask, kl)
+    if window is None:
+        attn.attn_fwd(qd, kd, vd, out, lse, scale, mask, kl)
+    else:
+        attn.attn_fwd_local(qd, kd, vd, out, window, lse, scale, mask, kl)
     ws = torch.empty(attn.attn_bwd_workspace_size(B, H, n_q, d, flags), dtype=torch.uint8, device="cuda")
     dq, dk, dv = torch.full_like(qd, float("nan")), torch.full_like(kd, float("nan")), torch.full_like(vd, float("nan"))
-    attn.attn_bwd(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, scale, mask, kl, flags=flags)
+    if window is None:
+        attn.attn_bwd(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, scale, mask, kl, flags=flags)
+    else:
+        attn.attn_bwd_local(qd, kd, vd, out, gd, lse, dq, dk, dv, ws, window, scale, mask, kl, flags=flags)
     torch.cuda.synchronize()
     f = lambda t: t.float().cpu().numpy().astype(np.float64)
     return (f(dq), f(dk), f(dv)), f(out)
 
 
-def bounds(orc, q, k, v, dout, scale, mask, lens, ref, out_dev, P=None, lse=None):
+def bounds(orc, q, k, v, dout, scale, mask, lens, ref, out_dev, P=None, lse=None, window=0):
     """(worst-case bounds, quadrature bounds) of the CUDA path's error, per element
-    (module docstring). P and lse, the oracle's weights and log-sum-exp, may be given."""
+    (module docstring). P and lse, the oracle's weights and log-sum-exp, may be given;
+    window as in the oracle (0: none)."""
     if P is None:
-        P = orc.attention_weights(q, k, scale, mask, lens)
+        P = orc.attention_weights(q, k, scale, mask, lens, window=window)
     if lse is None:
-        _, lse = orc.attention(q, k, v, scale, mask, lens)
+        _, lse = orc.attention(q, k, v, scale, mask, lens, window=window)
     Q, K, V, G = (bits_to_f64(x) for x in (q, k, v, dout))
     dq_r, dk_r, dv_r = ref
     d, n_q, n_k = Q.shape[-1], Q.shape[-2], K.shape[-2]
@@ -144,13 +152,15 @@ def check(got, ref, bnd):
             f"{name}: ||err|| {np.linalg.norm(err):.3e} above the quadrature bound {np.linalg.norm(qb):.3e}")
 
 
-def parity(orc, seed, B, H, n_q, n_k, d, mask, lens=None, scale=None, flags=0):
+def parity(orc, seed, B, H, n_q, n_k, d, mask, lens=None, scale=None, flags=0, window=None):
     q, k, v, dout, lens = draw(seed, B, H, n_q, n_k, d, mask, lens)
     scale = W.default_scale(d) if scale is None else scale
-    got, out_dev = run_bwd(q, k, v, dout, scale, mask, lens, flags)
+    got, out_dev = run_bwd(q, k, v, dout, scale, mask, lens, flags, window)
     kl = lens if mask & W.MASK_KEY_PADDING else None
-    ref = orc.attention_bwd(q, k, v, dout, scale, mask, kl)
-    bnd = bounds(orc, q, k, v, dout, scale, mask, kl, ref, out_dev)
+    # the oracle applies its window under the MASK_WINDOW bit
+    omask, ow = (mask, 0) if window is None else (mask | W.MASK_WINDOW, window)
+    ref = orc.attention_bwd(q, k, v, dout, scale, omask, kl, window=ow)
+    bnd = bounds(orc, q, k, v, dout, scale, omask, kl, ref, out_dev, window=ow)
     RESULTS.append(((B, H, n_q, n_k, d, mask), ratios(got, ref, bnd)))
     check(got, ref, bnd)
     return got, ref
@@ -228,6 +238,34 @@ def test_bwd_long_sequence(orc, d, mask):
     bnd = bounds(orc, q, k, v, dout, w.scale, mask, None, ref, out_dev)
     RESULTS.append(((1, 2, 4096, 4096, d, mask), ratios(got, ref, bnd)))
     check(got, ref, bnd)
+
+
+@pytest.mark.parametrize("d,flags", [(64, 0), (64, attn.BWD_DETERMINISTIC), (128, 0)])
+@pytest.mark.parametrize("window", [0, 1, 100, 127, 128, 300])
+@pytest.mark.parametrize("mask", [W.MASK_NONE, W.MASK_CAUSAL])
+def test_bwd_local_window(orc, d, flags, window, mask):
+    """attn_bwd_local against the oracle's gradients under its window mask: windows
+    inside one tile, at a tile edge and spanning several; n = 460 leaves a ragged tail."""
+    parity(orc, 7000 + d + window + mask + flags, 1, 2, 460, 460, d, mask, flags=flags, window=window)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_local_window_key_padding(orc, d):
+    """Window and key padding together; one batch entry's keys end inside the window of
+    the last rows, the other's at a tile edge."""
+    parity(orc, 7100 + d, 2, 2, 400, 400, d, W.MASK_KEY_PADDING | W.MASK_CAUSAL, lens=[300, 256], window=90)
+    parity(orc, 7150 + d, 2, 1, 400, 400, d, W.MASK_KEY_PADDING, lens=[37, 400], window=200)
+
+
+def test_bwd_local_window_covering_everything_equals_attn_bwd():
+    """A window at least n - 1 wide is no restriction: attn_bwd_local equals attn_bwd bit
+    for bit on dK and dV (the deterministic schedule: dQ too)."""
+    q, k, v, dout, lens = draw(7200, 1, 2, 300, 300, 64, W.MASK_CAUSAL)
+    scale = W.default_scale(64)
+    a, _ = run_bwd(q, k, v, dout, scale, W.MASK_CAUSAL, lens, attn.BWD_DETERMINISTIC)
+    b, _ = run_bwd(q, k, v, dout, scale, W.MASK_CAUSAL, lens, attn.BWD_DETERMINISTIC, window=299)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
 
 
 def test_bwd_rejects_small_workspace():

@@ -58,6 +58,9 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp,
                                ctypes.c_size_t, vp]
         L.attn_bwd.restype = i
+        L.attn_bwd_local.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, i, vp,
+                                     ctypes.c_size_t, vp]
+        L.attn_bwd_local.restype = i
         L.attn_bwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i]
         L.attn_bwd_host_workspace_size.restype = ctypes.c_size_t
         L.attn_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp,
@@ -290,6 +293,35 @@ def attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, scale=None, mask_mo
                         _ptr(workspace), nbytes, _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_local(q, k, v, out, dout, lse, dq, dk, dv, workspace, window, scale=None, mask_mode=MASK_NONE,
+                   key_lens=None, stream=None, flags=0):
+    """Gradients of attn_fwd_local (key j legal for query i only if |i - j| <= window, plus
+    mask_mode); arguments and workspace as in attn_bwd, with n_q = n_k."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, torch.bfloat16)
+    B, H, n, d_k = q.shape
+    d_v = v.shape[3]
+    if (k.shape != (B, H, n, d_k) or v.shape != (B, H, n, d_v) or out.shape != (B, H, n, d_v)
+            or dout.shape != out.shape or dq.shape != q.shape or dk.shape != k.shape or dv.shape != v.shape):
+        raise ValueError("local attention is self-attention: q, k, v, out, dout and the gradients share B, H, n")
+    _check(lse, "lse", torch.float32, 3)
+    if lse.shape != (B, H, n):
+        raise ValueError("lse must have shape [B, H, n]")
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, 1)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib().attn_bwd_local(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                              _ptr(dv), B, H, n, d_k, d_v, float(scale), int(window), int(mask_mode), _ptr(key_lens),
+                              int(flags), _ptr(workspace), nbytes, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_local")
     return dq, dk, dv
 
 

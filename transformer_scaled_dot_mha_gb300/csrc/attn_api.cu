@@ -189,6 +189,27 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   return attn::launch_attn_bwd(a, enc, workspace);
 }
 
+int attn_bwd_local(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int h, int n, int d_k, int d_v,
+                   float scale, int window, int mask_mode, const int32_t* key_lens, int flags, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  int st = check_common(q, k, v, out, lse, B, h, n, n, d_k, d_v, scale, mask_mode, key_lens);
+  if (st != ATTN_OK) return st;
+  if (window < 0) return ATTN_ERR_INVALID;
+  if (!dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID;
+  if (flags & ~ATTN_BWD_DETERMINISTIC) return ATTN_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 16))
+    return ATTN_ERR_INVALID;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < attn::bwd_workspace_bytes(B, h, n, d_k, flags)) return ATTN_ERR_INVALID;
+  attn::PFN_encodeTiled enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::BwdArgs a{q, k, v, out, dout, lse, dq, dk, dv, B, h, n, n, d_k, scale, mask_mode, key_lens,
+                  static_cast<cudaStream_t>(stream), flags, window};
+  return attn::launch_attn_bwd(a, enc, workspace);
+}
+
 size_t attn_bwd_host_workspace_size(int B, int h, int n_q, int n_k, int d, int mask_mode, int flags) {
   if (B <= 0 || h <= 0 || n_q <= 0 || n_k <= 0 || (d != 64 && d != 128)) return 0;
   if (mask_mode < 0 || mask_mode > (ATTN_MASK_CAUSAL | ATTN_MASK_KEY_PADDING)) return 0;

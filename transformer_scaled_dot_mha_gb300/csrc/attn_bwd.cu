@@ -122,7 +122,8 @@ struct BwdParams {
   uint16_t* g1;        // dkdv: dV [BH][n_k][D]
   const int32_t* key_lens;
   int H, n_q, n_k, mask_mode, BH, tiles, q_tiles;
-  int group;  // heads per group of the CTA order (see the kernel)
+  int group;   // heads per group of the CTA order (see the kernel)
+  int window;  // local window: key j legal for query i only if |i - j| <= window; -1: none
   float scale, scale_log2;
 };
 
@@ -262,15 +263,20 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
   int kv_len = p.n_k;
   if (p.mask_mode & 2) kv_len = min(max(p.key_lens[b], 0), p.n_k);
   const int own0 = own * T;
-  // streamed tiles [s_begin, s_end)
+  const int window = p.window;
+  // streamed tiles [s_begin, s_end): the tiles holding a row some own row may pair with
   int s_begin, s_end;
-  if (DKDV) {  // query tiles that see any key of [own0, own0 + T)
-    s_begin = (causal ? own0 : 0) / T;
-    s_end = (own0 < kv_len) ? (p.n_q + T - 1) / T : s_begin;
-  } else {     // key tiles any query of [own0, own0 + T) sees
-    s_begin = 0;
-    const int hi = causal ? min(kv_len, own0 + T) : kv_len;
-    s_end = (own0 < p.n_q) ? (hi + T - 1) / T : 0;
+  if (DKDV) {  // queries [lo, hi) that see a key of [own0, own0 + T)
+    const int lo = causal ? own0 : (window >= 0 ? max(0, own0 - window) : 0);
+    const int hi = window >= 0 ? min(p.n_q, own0 + T + window) : p.n_q;
+    s_begin = min(lo, p.n_q) / T;
+    s_end = (own0 < kv_len && lo < hi) ? (hi + T - 1) / T : s_begin;
+  } else {     // keys [lo, hi) that a query of [own0, own0 + T) sees
+    const int lo = window >= 0 ? max(0, own0 - window) : 0;
+    int hi = causal ? min(kv_len, own0 + T) : kv_len;
+    if (window >= 0) hi = min(hi, own0 + T + window);
+    s_begin = min(lo, kv_len) / T;
+    s_end = (own0 < p.n_q && lo < hi) ? (hi + T - 1) / T : s_begin;
   }
   const int n_s = max(0, s_end - s_begin);
 
@@ -522,16 +528,25 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
     const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     // dQ: this thread's query statistics
     uint64_t nl2 = 0ull, nd2 = 0ull;  // (-lse*log2e, -lse*log2e), (-D, -D)
-    int my_lim = 0;                   // keys [0, my_lim) are legal for this query
+    // the rows this thread's row pairs with: [my_lo, my_hi) (keys for dQ, queries for dK/dV)
+    int my_lo = 0, my_hi = 0;
     if (!DKDV && own_row < p.n_q) {
       const float* srow = p.stats + ((size_t)bh * p.q_tiles + own) * 2 * T + r;
       const float nl = srow[0];
       const float nd = srow[T];
       nl2 = ptx::f2_pack(nl, nl);
       nd2 = ptx::f2_pack(nd, nd);
-      my_lim = key_limit(own_row, kv_len, causal);
+      my_hi = key_limit(own_row, kv_len, causal);
+      if (window >= 0) {
+        my_lo = max(0, own_row - window);
+        my_hi = min(my_hi, own_row + window + 1);
+      }
     }
-    const bool row_dead = DKDV ? own_row >= kv_len : my_lim == 0;
+    if (DKDV && own_row < kv_len) {  // query >= key (causal), |query - key| <= window
+      my_lo = causal ? own_row : (window >= 0 ? max(0, own_row - window) : 0);
+      my_hi = window >= 0 ? own_row + window + 1 : 0x7fffffff;  // rows past n_q carry P = 0
+    }
+    const bool row_dead = my_lo >= my_hi;
     bool ok = true;
     for (int u = 0; u < n_s && ok; ++u) {
       const int st = u % STAGES;
@@ -542,12 +557,10 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
       ptx::tc_fence_after();
       const int s0 = (s_begin + u) * T + g * 64;  // streamed row of this thread's first column
       // columns [lo, hi) are legal for this thread; the rest get P = 0
-      int lo = 0, hi = 64;
-      if (DKDV) {
-        if (row_dead) hi = 0;
-        else if (causal) lo = max(0, own_row - s0);  // query >= key
-      } else {
-        hi = max(0, min(64, my_lim - s0));
+      int lo = 0, hi = 0;
+      if (!row_dead) {
+        lo = max(0, my_lo - s0);
+        hi = (int)max(0LL, min(64LL, (long long)my_hi - s0));
       }
       const bool full = (lo == 0 && hi == 64);
       const float* vnl = vec + st * 2 * T + g * 64;      // -lse*log2e of the columns (DKDV)
@@ -762,6 +775,7 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_ac
   p.mask_mode = a.mask_mode;
   p.BH = BH;
   p.group = BH < kHeadGroup ? (int)BH : kHeadGroup;
+  p.window = a.window;
   p.scale = a.scale;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634074);
   // dK, dV: own = key tiles; A0 = K, A1 = V; streamed R0 = Q, R1 = dO

@@ -87,7 +87,8 @@ struct BwdArgs {
   int mask_mode;
   const int32_t* key_lens;
   cudaStream_t stream;
-  int flags = 0;  // ATTN_BWD_DETERMINISTIC
+  int flags = 0;    // ATTN_BWD_DETERMINISTIC
+  int window = -1;  // local-window radius (>= 0), or -1 for none
 };
 
 // Validated arguments of one multi-head layer call (d_k == d_v == d).
