@@ -17,9 +17,9 @@ on the device);
 FLOPs are algorithmic: 2 d_model h d per projected row for each of the four
 projections plus the attention's.
 
---grad times the gradients instead (one attn_bwd call per step: D = rowsum(dO*O),
-the dK/dV kernel and the dQ kernel), given the forward's output and lse computed
-once before the timed region; FLOPs are algorithmic, 2 (3 d_k + 2 d_v) per legal
+--grad times the gradients instead (one attn_bwd call per step, attn_bwd_local for
+the local-window workload: D = rowsum(dO*O), the dK/dV kernel and the dQ kernel),
+given the forward's output and lse computed once before the timed region; FLOPs are algorithmic, 2 (3 d_k + 2 d_v) per legal
 pair (the five products of the backward pass).
 
 Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
@@ -73,6 +73,8 @@ class L2Flush:
     def __call__(self):
         self.buf.zero_()
         self.sink.copy_(self.words.sum())
+
+
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
@@ -94,8 +96,9 @@ NCU_TRAFFIC = {
     ("local_causal_b2_h16_n8192_d64_w511", "attn_fwd_tc_kernel", "dd287655676f270e"): 110697472,
     # the warp kernel only (the merge kernel is not counted)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "15a9265a513b2001"): 424486400,
-    # the fused d = 64 kernel
-    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "caee004531853f22"): 291833088,
+    # the fused d = 64 kernel (the local-window workload: its LOCAL instantiation)
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "95d193a62441cd41"): 292000512,
+    ("local_causal_b2_h16_n8192_d64_w511", "attn_bwd_tc_kernel", "95d193a62441cd41"): 290847488,
 }
 
 

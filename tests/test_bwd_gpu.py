@@ -263,9 +263,10 @@ def test_bwd_local_window_covering_everything_equals_attn_bwd():
     q, k, v, dout, lens = draw(7200, 1, 2, 300, 300, 64, W.MASK_CAUSAL)
     scale = W.default_scale(64)
     a, _ = run_bwd(q, k, v, dout, scale, W.MASK_CAUSAL, lens, attn.BWD_DETERMINISTIC)
-    b, _ = run_bwd(q, k, v, dout, scale, W.MASK_CAUSAL, lens, attn.BWD_DETERMINISTIC, window=299)
-    for x, y in zip(a, b):
-        assert np.array_equal(x, y)
+    for window in (299, 2**31 - 1):  # n - 1, and the widest window an int holds
+        b, _ = run_bwd(q, k, v, dout, scale, W.MASK_CAUSAL, lens, attn.BWD_DETERMINISTIC, window=window)
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
 
 
 def test_bwd_rejects_small_workspace():

@@ -64,6 +64,8 @@ def test_local_window_covering_everything_equals_attn_fwd():
     a, _ = run_local(q, k, v, kl, w.scale, 400, C)
     b = attn.attention(dev_bf16(q), dev_bf16(k), dev_bf16(v), w.scale, C).float().cpu().numpy()
     assert np.array_equal(a, b)
+    c, _ = run_local(q, k, v, kl, w.scale, 2**31 - 1, C)  # the widest window an int holds
+    assert np.array_equal(a, c)
 
 
 def test_local_full_size_sampled_rows(orc):

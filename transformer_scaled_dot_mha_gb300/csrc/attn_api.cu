@@ -104,6 +104,7 @@ int attn_fwd_local(const void* q, const void* k, const void* v, void* out, float
   int st = check_common(q, k, v, out, lse, B, h, n, n, d_k, d_v, scale, mask_mode, key_lens);
   if (st != ATTN_OK) return st;
   if (window < 0) return ATTN_ERR_INVALID;
+  window = window < n ? window : n;  // |i - j| < n always: a wider window is the same mask
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return ATTN_ERR_INVALID;
   if (d_k != d_v || (d_k != 64 && d_k != 128)) return ATTN_ERR_UNSUPPORTED;
   attn::PFN_encodeTiled enc = tensor_map_encoder();
@@ -196,6 +197,7 @@ int attn_bwd_local(const void* q, const void* k, const void* v, const void* out,
   int st = check_common(q, k, v, out, lse, B, h, n, n, d_k, d_v, scale, mask_mode, key_lens);
   if (st != ATTN_OK) return st;
   if (window < 0) return ATTN_ERR_INVALID;
+  window = window < n ? window : n;  // |i - j| < n always: a wider window is the same mask
   if (!dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID;
   if (flags & ~ATTN_BWD_DETERMINISTIC) return ATTN_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||

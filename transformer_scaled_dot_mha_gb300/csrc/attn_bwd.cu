@@ -220,8 +220,10 @@ __device__ __forceinline__ int key_limit(int i, int kv_len, bool causal) { retur
 
 // ------------------------------------------------------------------ dK, dV
 // KV tile kt of head bh; query tiles it = q_begin .. tiles-1 (causal: those at or
-// after the key tile). MODE selects the operand roles (see the file comment).
-template <int D, bool DKDV, bool FUSED = false>
+// after the key tile). MODE selects the operand roles (see the file comment). LOCAL:
+// the local-window instantiation; the others see a constant window of -1, so their
+// tile ranges and column bounds fold to the full-attention forms.
+template <int D, bool DKDV, bool FUSED = false, bool LOCAL = false>
 __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                        const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
   int kv_len = p.n_k;
   if (p.mask_mode & 2) kv_len = min(max(p.key_lens[b], 0), p.n_k);
   const int own0 = own * T;
-  const int window = p.window;
+  const int window = LOCAL ? p.window : -1;
   // streamed tiles [s_begin, s_end): the tiles holding a row some own row may pair with
   int s_begin, s_end;
   if (DKDV) {  // queries [lo, hi) that see a key of [own0, own0 + T)
@@ -557,11 +559,14 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
       ptx::tc_fence_after();
       const int s0 = (s_begin + u) * T + g * 64;  // streamed row of this thread's first column
       // columns [lo, hi) are legal for this thread; the rest get P = 0
-      int lo = 0, hi = 0;
-      if (!row_dead) {
+      int lo = 0, hi = 64;
+      if (LOCAL || !DKDV) {  // my_hi - s0 stays in range: the window is at most n
         lo = max(0, my_lo - s0);
-        hi = (int)max(0LL, min(64LL, (long long)my_hi - s0));
+        hi = max(0, min(64, my_hi - s0));
+      } else if (causal) {  // query >= key
+        lo = max(0, my_lo - s0);
       }
+      if (row_dead) hi = 0;
       const bool full = (lo == 0 && hi == 64);
       const float* vnl = vec + st * 2 * T + g * 64;      // -lse*log2e of the columns (DKDV)
       const float* vnd = vec + st * 2 * T + T + g * 64;  // -D of the columns (DKDV)
@@ -721,13 +726,13 @@ CUresult encode(PFN_encodeTiled enc, CUtensorMap* map, const void* base, int d, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <int D, bool DKDV, bool FUSED = false>
+template <int D, bool DKDV, bool FUSED, bool LOCAL>
 int set_smem_attr() {
   static std::atomic<bool> done[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   if (!done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<D, DKDV, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_bwd_tc_kernel<D, DKDV, FUSED, LOCAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              BCfg<D, FUSED>::SMEM_BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
     done[dev].store(true, std::memory_order_release);
@@ -737,7 +742,7 @@ int set_smem_attr() {
 
 // dq_acc: the fp32 dQ accumulator of the fused schedule, or null for the
 // deterministic one.
-template <int D>
+template <int D, bool LOCAL>
 int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_acc) {
   const int BH = a.B * a.H;
   const bool fused = dq_acc != nullptr;
@@ -749,11 +754,11 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_ac
   if (!fused) macc = mq;  // not read by the deterministic kernels
   if (fused) {
     if constexpr (D == 64) {
-      if (set_smem_attr<D, true, true>() != ATTN_OK) return ATTN_ERR_CUDA;
+      if (set_smem_attr<D, true, true, LOCAL>() != ATTN_OK) return ATTN_ERR_CUDA;
     } else {
       return ATTN_ERR_UNSUPPORTED;
     }
-  } else if (set_smem_attr<D, true>() != ATTN_OK || set_smem_attr<D, false>() != ATTN_OK) {
+  } else if (set_smem_attr<D, true, false, LOCAL>() != ATTN_OK || set_smem_attr<D, false, false, LOCAL>() != ATTN_OK) {
     return ATTN_ERR_CUDA;
   }
   if (fused && cudaMemsetAsync(dq_acc, 0, (size_t)BH * a.n_q * D * sizeof(float), a.stream) != cudaSuccess)
@@ -787,8 +792,8 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_ac
   if (fused) {
     if constexpr (D == 64) {
       using CF = BCfg<D, true>;
-      attn_bwd_tc_kernel<D, true, true><<<(unsigned)grid, CF::THREADS, CF::SMEM_BYTES, a.stream>>>(mk, mv, mq, mdo,
-                                                                                                   macc, p);
+      attn_bwd_tc_kernel<D, true, true, LOCAL><<<(unsigned)grid, CF::THREADS, CF::SMEM_BYTES, a.stream>>>(
+          mk, mv, mq, mdo, macc, p);
       if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
       const long long n4 = (long long)BH * a.n_q * D / 4;
       const long long blocks = std::min<long long>((n4 + 255) / 256, 152LL * 8);
@@ -797,8 +802,8 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_ac
       return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     }
   }
-  attn_bwd_tc_kernel<D, true><<<(unsigned)grid, BCfg<D>::THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mk, mv, mq, mdo,
-                                                                                                  macc, p);
+  attn_bwd_tc_kernel<D, true, false, LOCAL><<<(unsigned)grid, BCfg<D>::THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(
+      mk, mv, mq, mdo, macc, p);
   if (cudaPeekAtLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   // dQ: own = query tiles; A0 = Q, A1 = dO; streamed R0 = K, R1 = V
   p.g0 = static_cast<uint16_t*>(a.dq);
@@ -806,8 +811,8 @@ int launch_bwd(const BwdArgs& a, PFN_encodeTiled enc, float* stats, float* dq_ac
   p.tiles = (a.n_q + T - 1) / T;
   grid = (long long)BH * p.tiles;
   if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  attn_bwd_tc_kernel<D, false><<<(unsigned)grid, BCfg<D>::THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(mq, mdo, mk, mv,
-                                                                                                   macc, p);
+  attn_bwd_tc_kernel<D, false, false, LOCAL><<<(unsigned)grid, BCfg<D>::THREADS, BCfg<D>::SMEM_BYTES, a.stream>>>(
+      mq, mdo, mk, mv, macc, p);
   return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -825,8 +830,11 @@ size_t bwd_workspace_bytes(int B, int H, int n_q, int d, int flags) {
 int launch_attn_bwd(const BwdArgs& a, PFN_encodeTiled enc, void* workspace) {
   float* stats = static_cast<float*>(workspace);
   float* dq_acc = bwd_fused(a.d, a.flags) ? stats + (size_t)a.B * a.H * ((a.n_q + T - 1) / T) * 2 * T : nullptr;
-  if (a.d == 64) return launch_bwd<64>(a, enc, stats, dq_acc);
-  if (a.d == 128) return launch_bwd<128>(a, enc, stats, nullptr);
+  const bool local = a.window >= 0;
+  if (a.d == 64)
+    return local ? launch_bwd<64, true>(a, enc, stats, dq_acc) : launch_bwd<64, false>(a, enc, stats, dq_acc);
+  if (a.d == 128)
+    return local ? launch_bwd<128, true>(a, enc, stats, nullptr) : launch_bwd<128, false>(a, enc, stats, nullptr);
   return ATTN_ERR_UNSUPPORTED;
 }
 
