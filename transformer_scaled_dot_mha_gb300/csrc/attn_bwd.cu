@@ -577,13 +577,18 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
         ptx::tmem_ld32(t_y + ch * 32, ys);
         ptx::tmem_wait_ld();
         uint32_t pw[16], dw[16];
+        float4 nl4, nd4;  // DKDV: -lse*log2e and -D of four columns, one 16-byte broadcast load each
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
           const int cc = ch * 32 + x;  // column within this warpgroup's half
           uint64_t nl, nd;
           if (DKDV) {
-            nl = *reinterpret_cast<const uint64_t*>(vnl + cc);
-            nd = *reinterpret_cast<const uint64_t*>(vnd + cc);
+            if ((x & 2) == 0) {
+              nl4 = *reinterpret_cast<const float4*>(vnl + cc);
+              nd4 = *reinterpret_cast<const float4*>(vnd + cc);
+            }
+            nl = (x & 2) ? ptx::f2_pack(nl4.z, nl4.w) : ptx::f2_pack(nl4.x, nl4.y);
+            nd = (x & 2) ? ptx::f2_pack(nd4.z, nd4.w) : ptx::f2_pack(nd4.x, nd4.y);
           } else {
             nl = nl2;
             nd = nd2;
