@@ -80,10 +80,10 @@ def test_linear_matches_oracle(orc, M, N, K, bias):
 
 
 def test_linear_cluster_path_odd_row_blocks(orc):
-    """A launch of at least 1024 tiles runs as 2-CTA clusters (row blocks 2u, 2u + 1
-    share each W tile). 33 row blocks (M = 4103) x 32 column blocks: the last pair's
-    second CTA lies wholly past M and must write nothing; sampled rows of every row
-    block edge against the oracle, and the rows past M of a guarded buffer untouched."""
+    """A launch of many tiles runs on 2-CTA clusters (row blocks 2u, 2u + 1 together).
+    33 row blocks (M = 4103) x 32 column blocks: the last pair's second CTA lies wholly
+    past M and must write nothing; sampled rows of every row block edge against the
+    oracle, and the rows past M of a guarded buffer untouched."""
     M, N, K = 4103, 8192, 64
     x, w, b = draw(9300, M, N, K)
     pad_rows = 40
@@ -93,6 +93,25 @@ def test_linear_cluster_path_odd_row_blocks(orc):
     torch.cuda.synchronize()
     assert torch.all(buf[M * N:] == -7.0)
     rows = sorted({0, 1, 127, 128, M // 2, 4095, 4096, M - 2, M - 1} | set(range(5, M, 37)))
+    check(orc, x, w, b, y.float().cpu().numpy().astype(np.float64), np.array(rows))
+
+
+def test_linear_pair_path_tails(orc):
+    """A launch of at least 512 tiles runs the 2-SM MMA (two CTAs of a cluster, one
+    M256 N256 MMA stream on both SMs). 33 row blocks (M = 4100: the last pair's first
+    CTA holds 4 rows, its second none), 17 column blocks (N = 4104: the last holds 8
+    columns, so the second CTA's half of that W tile lies wholly past N), K = 200 (a
+    K tail inside the fourth 64-deep step): sampled rows against the oracle, all
+    columns, and the rows past M of a guarded buffer untouched."""
+    M, N, K = 4100, 4104, 200
+    x, w, b = draw(9400, M, N, K)
+    pad_rows = 40
+    buf = torch.full(((M + pad_rows) * N,), -7.0, dtype=torch.bfloat16, device="cuda")
+    y = buf[:M * N].view(M, N)
+    attn.attn_linear(dev(x), dev(w), y, dev(b))
+    torch.cuda.synchronize()
+    assert torch.all(buf[M * N:] == -7.0)
+    rows = sorted({0, 1, 127, 128, 255, 256, M // 2, 4095, 4096, M - 1} | set(range(7, M, 41)))
     check(orc, x, w, b, y.float().cpu().numpy().astype(np.float64), np.array(rows))
 
 
