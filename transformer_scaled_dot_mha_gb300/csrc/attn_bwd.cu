@@ -268,15 +268,23 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
   const int window = LOCAL ? p.window : -1;
   // streamed tiles [s_begin, s_end): the tiles holding a row some own row may pair with
   int s_begin, s_end;
-  if (DKDV) {  // queries [lo, hi) that see a key of [own0, own0 + T)
-    const int lo = causal ? own0 : (window >= 0 ? max(0, own0 - window) : 0);
-    const int hi = window >= 0 ? min(p.n_q, own0 + T + window) : p.n_q;
+  if constexpr (!LOCAL) {
+    if (DKDV) {  // query tiles that see any key of [own0, own0 + T)
+      s_begin = (causal ? own0 : 0) / T;
+      s_end = (own0 < kv_len) ? (p.n_q + T - 1) / T : s_begin;
+    } else {     // key tiles any query of [own0, own0 + T) sees
+      s_begin = 0;
+      const int hi = causal ? min(kv_len, own0 + T) : kv_len;
+      s_end = (own0 < p.n_q) ? (hi + T - 1) / T : 0;
+    }
+  } else if (DKDV) {  // queries [lo, hi) that see a key of [own0, own0 + T)
+    const int lo = causal ? own0 : max(0, own0 - window);
+    const int hi = min(p.n_q, own0 + T + window);
     s_begin = min(lo, p.n_q) / T;
     s_end = (own0 < kv_len && lo < hi) ? (hi + T - 1) / T : s_begin;
-  } else {     // keys [lo, hi) that a query of [own0, own0 + T) sees
-    const int lo = window >= 0 ? max(0, own0 - window) : 0;
-    int hi = causal ? min(kv_len, own0 + T) : kv_len;
-    if (window >= 0) hi = min(hi, own0 + T + window);
+  } else {            // keys [lo, hi) that a query of [own0, own0 + T) sees
+    const int lo = max(0, own0 - window);
+    const int hi = min(causal ? min(kv_len, own0 + T) : kv_len, own0 + T + window);
     s_begin = min(lo, kv_len) / T;
     s_end = (own0 < p.n_q && lo < hi) ? (hi + T - 1) / T : s_begin;
   }
@@ -539,16 +547,16 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
       nl2 = ptx::f2_pack(nl, nl);
       nd2 = ptx::f2_pack(nd, nd);
       my_hi = key_limit(own_row, kv_len, causal);
-      if (window >= 0) {
+      if (LOCAL) {
         my_lo = max(0, own_row - window);
         my_hi = min(my_hi, own_row + window + 1);
       }
     }
-    if (DKDV && own_row < kv_len) {  // query >= key (causal), |query - key| <= window
-      my_lo = causal ? own_row : (window >= 0 ? max(0, own_row - window) : 0);
-      my_hi = window >= 0 ? own_row + window + 1 : 0x7fffffff;  // rows past n_q carry P = 0
+    if (LOCAL && DKDV && own_row < kv_len) {  // query >= key (causal), |query - key| <= window
+      my_lo = causal ? own_row : max(0, own_row - window);
+      my_hi = own_row + window + 1;  // rows past n_q carry P = 0
     }
-    const bool row_dead = my_lo >= my_hi;
+    const bool row_dead = LOCAL ? my_lo >= my_hi : (DKDV ? own_row >= kv_len : my_hi == 0);
     bool ok = true;
     for (int u = 0; u < n_s && ok; ++u) {
       const int st = u % STAGES;
@@ -560,13 +568,19 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
       const int s0 = (s_begin + u) * T + g * 64;  // streamed row of this thread's first column
       // columns [lo, hi) are legal for this thread; the rest get P = 0
       int lo = 0, hi = 64;
-      if (LOCAL || !DKDV) {  // my_hi - s0 stays in range: the window is at most n
-        lo = max(0, my_lo - s0);
+      if constexpr (LOCAL) {  // my_hi - s0 stays in range: the window is at most n
+        if (row_dead) {
+          hi = 0;
+        } else {
+          lo = max(0, my_lo - s0);
+          hi = max(0, min(64, my_hi - s0));
+        }
+      } else if (DKDV) {
+        if (row_dead) hi = 0;
+        else if (causal) lo = max(0, own_row - s0);  // query >= key
+      } else {
         hi = max(0, min(64, my_hi - s0));
-      } else if (causal) {  // query >= key
-        lo = max(0, my_lo - s0);
       }
-      if (row_dead) hi = 0;
       const bool full = (lo == 0 && hi == 64);
       const float* vnl = vec + st * 2 * T + g * 64;      // -lse*log2e of the columns (DKDV)
       const float* vnd = vec + st * 2 * T + T + g * 64;  // -D of the columns (DKDV)
