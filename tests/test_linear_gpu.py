@@ -115,6 +115,21 @@ def test_linear_pair_path_tails(orc):
     check(orc, x, w, b, y.float().cpu().numpy().astype(np.float64), np.array(rows))
 
 
+def test_linear_pair_path_split_last_round(orc):
+    """When the grid's last round of tiles is partly filled and their halves fit in one
+    round, those tiles run as two 128-column halves (M256 N128 on the SM pair). 86 row
+    blocks (M = 11000: the last pair's second CTA lies past M) x 6 column blocks (N =
+    1288: the last holds 8 columns) = 258 pair tiles; on 76 SM pairs the last 30 run as
+    halves. K = 200 ends inside a 64-deep step. Sampled rows, denser over the last five
+    row pairs, against the oracle on all columns."""
+    M, N, K = 11000, 1288, 200
+    x, w, b = draw(9500, M, N, K)
+    y = run(x, w, b)
+    rows = sorted({0, 1, 255, 256, 9727, 9728, 9729, 10879, 10880, M - 1} | set(range(3, M, 97))
+                  | set(range(9728, M, 23)))
+    check(orc, x, w, b, y, np.array(rows))
+
+
 def test_linear_guard_bands_and_determinism():
     """Nothing is written outside y, and two calls give identical bits."""
     x, w, b = draw(9100, 300, 264, 136)

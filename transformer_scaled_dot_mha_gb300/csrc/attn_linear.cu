@@ -80,6 +80,7 @@ struct LCfg {
   static constexpr int SMEM_BYTES = OFF_ABORT + 4;
   // X K-major, W MN-major; the pair's MMA spans both CTAs' 128 rows
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, true);
+  static constexpr uint32_t IDESC_HALF = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN / 2, true);  // a half tile
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 constexpr int kMaxDevices = 64;
@@ -164,8 +165,23 @@ struct LinParams {
   LinProblem pr[3];
   int n_prob;
   int total_tiles;  // units of CL row blocks x one column block
+  int split_from;   // the walk's items from here on are half tiles, two per tile
+  int total_items;
   int interleave;  // all problems share M and N: list order (row unit, problem, column block)
 };
+
+// Item `it` of the walk -> its tile; half = -1 for the whole 256-column tile, else 0 or
+// 1 for its columns [0, 128) or [128, 256). The tiles of a last, partly filled round of
+// the grid are split in two, so that round takes half as long on twice as many SMs.
+__device__ __forceinline__ int item_tile(const LinParams& p, int it, int& half) {
+  if (it < p.split_from) {
+    half = -1;
+    return it;
+  }
+  const int h = it - p.split_from;
+  half = h & 1;
+  return p.split_from + (h >> 1);
+}
 
 // cluster: acquire at cluster scope (arrivals that come from the other CTA of a pair)
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -297,10 +313,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol = ptx::policy_evict_last();  // X rows and W are each read by several CTAs
       uint32_t it = 0;
       bool ok = true;
-      for (int t = unit0; t < p.total_tiles && ok; t += units_step) {
-        int z, mu, nb;
-        tile_of(p, t, z, mu, nb);
+      for (int i = unit0; i < p.total_items && ok; i += units_step) {
+        int z, mu, nb, half;
+        tile_of(p, item_tile(p, i, half), z, mu, nb);
         const int mb = mu * CL + rank;
+        const int col_base = nb * BN + (half > 0 ? BN / 2 : 0);
+        const int boxes = (half >= 0 ? BN / 2 : BN) / CL / 64;  // W boxes this CTA loads per K step
         const CUtensorMap* tx = z == 0 ? &tm_x0 : z == 1 ? &tm_x1 : &tm_x2;
         const CUtensorMap* tw = z == 0 ? &tm_w0 : z == 1 ? &tm_w1 : &tm_w2;
         const int k_steps = (p.pr[z].K + BK - 1) / BK;
@@ -312,19 +330,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if constexpr (PAIR) {  // both CTAs' boxes counted on CTA 0's barrier
             const uint32_t full0 = cluster_addr(bar(B_FULL + s), 0);
-            if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FULL + s), 2 * (A_BYTES + B_BYTES));
+            if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_FULL + s), 2 * (A_BYTES + boxes * B_BOX_BYTES));
             tma_load_2d_pair(s_a + s * A_BYTES, tx, full0, kb * BK, mb * BM, pol);
-#pragma unroll
-            for (int c = 0; c < BN / 2 / 64; ++c)
-              tma_load_2d_pair(s_b + s * B_BYTES + c * B_BOX_BYTES, tw, full0, nb * BN + rank * (BN / 2) + c * 64,
+            for (int c = 0; c < boxes; ++c)
+              tma_load_2d_pair(s_b + s * B_BYTES + c * B_BOX_BYTES, tw, full0, col_base + (rank * boxes + c) * 64,
                                kb * BK, pol);
             continue;
           }
-          ptx::mbar_arrive_expect_tx(bar(B_FULL + s), A_BYTES + B_BYTES);
+          ptx::mbar_arrive_expect_tx(bar(B_FULL + s), A_BYTES + boxes * B_BOX_BYTES);
           ptx::tma_load_2d(s_a + s * A_BYTES, tx, bar(B_FULL + s), kb * BK, mb * BM, pol);
-#pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            ptx::tma_load_2d(s_b + s * B_BYTES + c * B_BOX_BYTES, tw, bar(B_FULL + s), nb * BN + c * 64, kb * BK, pol);
+          for (int c = 0; c < boxes; ++c)
+            ptx::tma_load_2d(s_b + s * B_BYTES + c * B_BOX_BYTES, tw, bar(B_FULL + s), col_base + c * 64, kb * BK, pol);
         }
       }
       if (!ok && (!PAIR || rank == 0)) {
@@ -341,9 +357,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t it = 0;
       int lt = 0;
       bool ok = true;
-      for (int t = unit0; t < p.total_tiles && ok; t += units_step, ++lt) {
-        int z, mu, nb;
-        tile_of(p, t, z, mu, nb);
+      for (int i = unit0; i < p.total_items && ok; i += units_step, ++lt) {
+        int z, mu, nb, half;
+        tile_of(p, item_tile(p, i, half), z, mu, nb);
+        const uint32_t idesc = half >= 0 ? C::IDESC_HALF : C::IDESC;
         const int buf = lt & 1;
         ok = wait_bar(bar(B_ACC_EMPTY + buf), ((lt >> 1) & 1) ^ 1, abort_flag, PAIR);
         if (!ok) break;
@@ -361,9 +378,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t ad = ptx::sdesc_sw128(a_st + kk * 32, 16, 1024);
             const uint64_t bd = ptx::sdesc_sw128(b_st + kk * 2048, B_BOX_BYTES, 1024);
             if constexpr (PAIR)
-              mma_ss_pair(d, ad, bd, C::IDESC, (kb | kk) ? 1u : 0u);
+              mma_ss_pair(d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
             else
-              ptx::mma_ss(d, ad, bd, C::IDESC, (kb | kk) ? 1u : 0u);
+              ptx::mma_ss(d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
           }
           if constexpr (PAIR)
             mma_commit_pair(bar(B_EMPTY + s), kPeers);
@@ -393,10 +410,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t stg = s_base + C::OFF_STG + (warp - 2) * 2 * STG_BYTES;
     int sb = 0;  // staging slab to fill next
     int lt = 0;
-    for (int t = unit0; t < p.total_tiles; t += units_step, ++lt) {
-      int z, mu, nb;
-      tile_of(p, t, z, mu, nb);
+    for (int i = unit0; i < p.total_items; i += units_step, ++lt) {
+      int z, mu, nb, half;
+      tile_of(p, item_tile(p, i, half), z, mu, nb);
       const int mb = mu * CL + rank;
+      const int col_base = nb * BN + (half > 0 ? BN / 2 : 0);
       const int buf = lt & 1;
       if (!__all_sync(0xffffffffu, wait_bar(bar(B_ACC_FULL + buf), (lt >> 1) & 1, abort_flag))) break;
       ptx::tc_fence_after();
@@ -405,12 +423,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       // rows of this warp's slabs inside Y (the second CTA of a pair can lie wholly past M)
       const bool row_ok = mb * BM + quarter * 32 < P.M;
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
+      for (int c = 0; c < (half >= 0 ? BN / 2 : BN) / 64; ++c) {
         uint32_t v[64];
         ptx::tmem_ld32(tmem + lane_off + buf * BN + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         ptx::tmem_ld32(tmem + lane_off + buf * BN + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         ptx::tmem_wait_ld();
-        const int col0 = nb * BN + c * 64;
+        const int col0 = col_base + c * 64;
         if (col0 < P.N && row_ok) {
           uint32_t w[32];
 #pragma unroll
@@ -558,7 +576,7 @@ int launch_linear_cl(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cud
     P.tile_begin = (int)tiles;
     const long long m_units = ((long long)(j.M + BM - 1) / BM + CL - 1) / CL;
     tiles += m_units * P.n_blocks;
-    if (tiles > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (tiles > 0x7fff0000LL) return ATTN_ERR_UNSUPPORTED;  // room for the split items
     same = same && j.M == jobs[0].M && j.N == jobs[0].N;
   }
   for (int z = n_jobs; z < 3; ++z) {  // unused slots repeat the first problem's maps
@@ -568,8 +586,13 @@ int launch_linear_cl(const LinearJob* jobs, int n_jobs, PFN_encodeTiled enc, cud
     p.pr[z] = p.pr[0];
   }
   p.total_tiles = (int)tiles;
+  // a last round of the grid that is partly filled: split its tiles when their halves
+  // fit in one round
+  const long long rem = tiles % clusters;
+  p.split_from = (int)((rem > 0 && 2 * rem <= clusters) ? tiles - rem : tiles);
+  p.total_items = p.split_from + 2 * (p.total_tiles - p.split_from);
   p.interleave = (n_jobs > 1 && same) ? 1 : 0;
-  const int grid = CL * (int)(tiles < clusters ? tiles : clusters);
+  const int grid = CL * (p.total_items < clusters ? p.total_items : clusters);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
