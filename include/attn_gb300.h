@@ -147,7 +147,8 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* out, float*
  * (ATTN_MASK_CAUSAL makes the window one-sided, i - window <= j <= i;
  * ATTN_MASK_KEY_PADDING as in attn_fwd). Self-attention only: q, k, v, out are
  * [B, h, n, d]. K/V tiles outside every row's window are never loaded.
- * window >= 0 (ATTN_ERR_INVALID otherwise); other rules as attn_fwd.
+ * window >= 0 (ATTN_ERR_INVALID otherwise); a window of n or more restricts nothing
+ * (|i - j| < n always). Other rules as attn_fwd.
  */
 int attn_fwd_local(const void* q, const void* k, const void* v, void* out, float* lse,
                    int B, int h, int n, int d_k, int d_v, float scale, int window,
@@ -275,12 +276,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
 
 /*
  * attn_bwd_local -- gradients of attn_fwd_local (restricted self-attention: key j is
- * legal for query i only if |i - j| <= window, together with mask_mode; SURVEY's f4
- * row, vlmlib.cn "restricted self-attention"), exactly as attn_bwd computes them for
+ * legal for query i only if |i - j| <= window, together with mask_mode; vlmlib.cn
+ * "restricted self-attention"), exactly as attn_bwd computes them for
  * attn_fwd: the same definitions, numerics, schedules, flags and workspace
  * (attn_bwd_workspace_size(B, h, n, d_k, flags)), with n_q = n_k = n and the window
  * entering P's mask. out and lse are those attn_fwd_local returned for the same
- * q, k, v, scale, window, mask_mode and key_lens. window < 0: ATTN_ERR_INVALID.
+ * q, k, v, scale, window, mask_mode and key_lens. window < 0: ATTN_ERR_INVALID; a
+ * window of n or more is the unrestricted mask (as in attn_fwd_local).
  * Key tiles no query of a query tile may see, and query tiles outside a key tile's
  * window, are skipped; every dq, dk, dv element is still written.
  */
