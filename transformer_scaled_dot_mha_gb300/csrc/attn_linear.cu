@@ -164,7 +164,7 @@ struct LinProblem {
 struct LinParams {
   LinProblem pr[3];
   int n_prob;
-  int total_tiles;  // units of CL row blocks x one column block
+  int total_tiles;  // a row block (a pair: two) x one column block each
   int split_from;   // the walk's items from here on are half tiles, two per tile
   int total_items;
   int interleave;  // all problems share M and N: list order (row unit, problem, column block)
@@ -208,7 +208,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (ptx::globaltimer_ns() - t0 > kDrainLimitNs) return;
 }
 
-// Tile t of the list -> problem z, row unit mu (CL row blocks), column block nb.
+// Tile t of the list -> problem z, row unit mu (one row block; a pair: two), column block nb.
 __device__ __forceinline__ void tile_of(const LinParams& p, int t, int& z, int& mb, int& nb) {
   if (p.interleave) {
     const int nbk = p.pr[0].n_blocks;
