@@ -365,8 +365,10 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
     // Half h of streamed tile u: S_h(u) and dP_h(u) (64 streamed rows), then, once its
     // warpgroup has stored P / dS, the accumulations. SPLIT: warp WARP_MMA + h serves
     // half h. Otherwise warp WARP_MMA serves both, in the order acc_h(u-1), S/dP_h(u)
-    // for h = 0, 1, and warp WARP_MMA + 1 idles.
-    if (lane == 0 && n_s > 0 && (SPLIT || warp == WARP_MMA)) {
+    // for h = 0, 1; FUSED: warp WARP_MMA + 1 issues dQ_u = dS_u K once both halves of
+    // tile u have stored dS (its own TMEM buffers: the other accumulators keep the
+    // order and bits of the single-issuer schedule), else it idles.
+    if (lane == 0 && n_s > 0 && (SPLIT || FUSED || warp == WARP_MMA)) {
       // Shared-memory descriptors are built once and advanced by adding (offset >> 4)
       // to the start-address field (addresses stay below 2^18, so the 14-bit field never
       // carries): this thread issues every MMA of the CTA and is kept lean.
@@ -420,7 +422,17 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
         }
       };
       bool ok = wait_bar(bar(C::B_AFULL), 0, abort_flag) && wait_bar(bar(C::B_FULL), 0, abort_flag);
-      if (SPLIT) {
+      if (FUSED && warp == WARP_MMA + 1) {
+        for (int w = 0; w < n_s && ok; ++w) {
+          // dS_w complete in shared memory (both halves); the buffer's previous partial
+          // (tile w - 2) read out of TMEM
+          ok = wait_bar(bar(C::B_PFULL), w & 1, abort_flag) && wait_bar(bar(C::B_PFULL + 1), w & 1, abort_flag);
+          if (ok && w >= 2) ok = wait_bar(bar(C::B_DQFREE + (w & 1)), ((w >> 1) - 1) & 1, abort_flag);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_dq(w);
+        }
+      } else if (SPLIT) {
         // this warp serves half hs only: acc_hs(u-1), then S/dP_hs(u)
         const int hs = warp - WARP_MMA;
         if (ok) {
@@ -456,22 +468,11 @@ __global__ void __launch_bounds__(BCfg<D, FUSED>::THREADS, 1)
           ptx::tc_fence_after();
           issue_acc(u - 1, h);
           if (h == 1) ptx::mma_commit(bar(C::B_EMPTY + (u - 1) % STAGES));  // tile u-1's stage is consumed
-          if (FUSED && h == 1) {
-            // dS_{u-1} is complete in shared memory; its buffer's previous partial
-            // (tile u-3) must have been read out
-            const int w = u - 1;
-            if (w >= 2) {
-              ok = wait_bar(bar(C::B_DQFREE + (w & 1)), ((w >> 1) - 1) & 1, abort_flag);
-              if (!ok) break;
-              ptx::tc_fence_after();
-            }
-            issue_dq(w);
-          }
           if (u < n_s) issue_sdp(u, h);
         }
       }
       }
-      if (ok) ptx::mma_commit(bar(C::B_ACC));
+      if (ok && !(FUSED && warp == WARP_MMA + 1)) ptx::mma_commit(bar(C::B_ACC));
       if (!ok) {
         ptx::mma_commit(bar(C::B_DRAIN + (warp - WARP_MMA)));
         drain_wait(bar(C::B_DRAIN + (warp - WARP_MMA)), 0);
