@@ -97,8 +97,8 @@ NCU_TRAFFIC = {
     # the warp kernel only (the merge kernel is not counted)
     ("decode_b16_h16_q1_k8192_d64", "attn_decode_warp_kernel", "15a9265a513b2001"): 424486400,
     # the fused d = 64 kernel (the local-window workload: its LOCAL instantiation)
-    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "ffe596777620d3be"): 291918848,
-    ("local_causal_b2_h16_n8192_d64_w511", "attn_bwd_tc_kernel", "ffe596777620d3be"): 290957568,
+    ("long_causal_b2_h16_n8192_d64", "attn_bwd_tc_kernel", "0aab31e7fb26f9cd"): 291646464,
+    ("local_causal_b2_h16_n8192_d64_w511", "attn_bwd_tc_kernel", "0aab31e7fb26f9cd"): 290630656,
 }
 
 
