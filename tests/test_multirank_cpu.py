@@ -75,3 +75,16 @@ def test_kernel_source_hash_ignores_comments_only():
     assert bench._code_only(code) == bench._code_only(code.replace("  return", "      return"))
     for k in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(k)) == 16
+
+
+def test_traffic_table_matches_current_sources():
+    """Every DRAM-traffic entry the bench can report was captured on the kernel sources
+    as they are now (its key is their hash) and names a defined workload: a kernel edit
+    leaves its entries stale until they are captured again."""
+    import bench
+    from transformer_scaled_dot_mha_gb300 import workloads as W
+
+    for (workload, kernel, src_hash), nbytes in bench.NCU_TRAFFIC.items():
+        assert workload in W.WORKLOADS
+        assert src_hash == bench.kernel_source_hash(kernel), (workload, kernel)
+        assert nbytes > 0
