@@ -26,7 +26,8 @@
 //                         query) and accumulates dQ += dS K_j.
 // The fused one (d = 64) computes each product once: the dK/dV kernel also writes
 // dS^T to shared memory and forms the partial dQ_i = dS_i K (one more MMA per
-// streamed tile, into one of two TMEM buffers); four drain warps move each partial
+// streamed tile, into one of two TMEM buffers, issued by a second MMA warp so that
+// one thread does not issue every MMA of the tile); four drain warps move each partial
 // through shared memory into an fp32 accumulator in global memory with TMA
 // reduce-adds, and attn_bwd_dq_convert_kernel scales and rounds it to bf16. Five
 // products instead of seven; the order of the reduce-adds, and so the last bits of
@@ -56,7 +57,8 @@ namespace {
 constexpr int T = 128;          // rows per tile (queries or keys)
 // warps 0-7 elementwise (two warpgroups, one per half of every streamed tile: its
 // rows 0-63 and 64-127), warp 8 TMA producer, warps 9 and 10 MMA issuers (one per
-// half; warp 9 serves both halves where the two halves' accumulators do not fit TMEM)
+// half for the dQ kernel at d = 128; elsewhere warp 9 serves both halves, and in the
+// fused kernel warp 10 issues the dQ partials)
 constexpr int EW_THREADS = 256;
 constexpr int WARP_LOAD = 8, WARP_MMA = 9;
 constexpr int WARP_DRAIN = 12;  // fused: warps 12-15 drain the dQ partials (warp 11 idles)
